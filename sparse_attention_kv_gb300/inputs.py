@@ -1,0 +1,171 @@
+"""Seeded synthetic inputs for block selection, shared by the tests, the smoke
+check and the benchmark.
+
+This module holds no arithmetic of the method: it only draws random arrays
+(numpy PCG64), rounds them to bf16 storage, and names the workload shapes.
+Both the CUDA path and the CPU oracle are fed from here.
+
+Workloads (synthetic stand-ins for the pages' bench data: queries, indexer
+heads and keys drawn i.i.d., one key per 64-token KV block, the last block
+partial when the context is not a multiple of 64):
+
+* ``tiny``   -- 1 query, 8 heads, fp32, 4,096 tokens (64 blocks), k = 16
+* ``decode`` -- 3 queries, 16 heads, bf16, capacity 262,144 tokens (4,096 blocks),
+  contexts 40K/64K/131K/258K tokens (+ 40,001 and 64,001), k = 32, no active count
+* ``prompt`` -- 256 queries, 16 heads, bf16, 131,072 tokens (2,048 blocks), k = 32
+* ``deep``   -- 256 queries, 16 heads, bf16, capacity 524,288 tokens (8,192 blocks),
+  contexts 262K/400K/520K tokens (up to 8,125 blocks), k = 32
+* ``stress`` -- 256 queries at 131,072 tokens: all-equal scores, 64-level scores,
+  w = 0, and per-query contexts of 1..2,048 blocks with a partial tail.
+
+"K" in a context size is decimal (520K = 520,000 tokens = 8,125 blocks), except
+131,072, which is written out.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_TOKENS = 64
+HEAD_DIM = 128
+F32 = 0
+BF16 = 1
+
+
+def blocks_for_tokens(tokens):
+    """Number of 64-token blocks covering ``tokens`` tokens (last one partial)."""
+    t = np.asarray(tokens, dtype=np.int64)
+    return ((t + BLOCK_TOKENS - 1) // BLOCK_TOKENS).astype(np.int32)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even (inputs are finite)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class Case:
+    """One synthetic selection problem.
+
+    ``q`` [nq,H,D] and ``kblk`` [C,D] hold fp32 values (dtype F32) or bf16 bit
+    patterns as uint16 (dtype BF16); ``w`` [nq,H] is fp32; ``n_blocks`` [nq]
+    int32.  ``tokens`` is the per-query context length the blocks cover.
+    """
+    q: np.ndarray
+    w: np.ndarray
+    kblk: np.ndarray
+    n_blocks: np.ndarray
+    tokens: np.ndarray
+    dtype: int
+    k: int
+    active_blocks: int = -1
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def nq(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def n_heads(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def max_blocks(self) -> int:
+        return self.kblk.shape[0]
+
+
+def make_case(seed: int, nq: int, n_heads: int, capacity_blocks: int, dtype: int,
+              tokens, k: int, *, active_blocks: int = -1, w_zero: bool = False,
+              kblk_equal: bool = False, name: str = "") -> Case:
+    """q, kblk ~ N(0,1), w ~ U(0,1) from ``seed``; ``tokens`` scalar or per query.
+
+    Rows of kblk at or past a query's block count are random too, so masking
+    is exercised.  bf16 storage rounds the fp32 draws to nearest even.
+    """
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((nq, n_heads, HEAD_DIM), dtype=np.float32)
+    kblk = rng.standard_normal((capacity_blocks, HEAD_DIM), dtype=np.float32)
+    w = rng.random((nq, n_heads), dtype=np.float32)
+    if w_zero:
+        w[:] = 0.0
+    if kblk_equal:
+        kblk[:] = kblk[0]
+    toks = np.broadcast_to(np.asarray(tokens, dtype=np.int64), (nq,)).copy()
+    n_blocks = blocks_for_tokens(toks)
+    if dtype == BF16:
+        q = to_bf16_bits(q)
+        kblk = to_bf16_bits(kblk)
+    return Case(q=q, w=w, kblk=kblk, n_blocks=n_blocks, tokens=toks, dtype=dtype, k=k,
+                active_blocks=active_blocks, name=name)
+
+
+def ragged_tokens(seed: int, nq: int, max_full_blocks: int) -> np.ndarray:
+    """Per-query contexts of U{1..max_full_blocks} blocks, the last one holding U{1..64} tokens."""
+    rng = np.random.default_rng(seed)
+    nb = rng.integers(1, max_full_blocks + 1, size=nq)
+    tail = rng.integers(1, BLOCK_TOKENS + 1, size=nq)
+    return (nb - 1) * BLOCK_TOKENS + tail
+
+
+def level_scores(seed: int, nq: int, cols: int, levels: int = 64) -> np.ndarray:
+    """Scores quantised to ``levels`` levels: floor(U * levels) / levels, fp32."""
+    rng = np.random.default_rng(seed)
+    u = rng.random((nq, cols))
+    return (np.floor(u * levels) / levels).astype(np.float32)
+
+
+def normal_scores(seed: int, nq: int, cols: int) -> np.ndarray:
+    """Continuous scores ~ N(0,1), fp32 (negative values included)."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((nq, cols), dtype=np.float32)
+
+
+# Named workloads: seed = 1000 * config index + sweep index.
+DECODE_TOKENS = (40_000, 40_001, 64_000, 64_001, 131_000, 258_000)
+DEEP_TOKENS = (262_000, 400_000, 520_000)
+
+
+def tiny_case() -> Case:
+    return make_case(1000, 1, 8, 64, F32, 4096, 16, name="tiny 1q x 8h fp32, 4,096 tokens")
+
+
+def decode_case(i: int) -> Case:
+    t = DECODE_TOKENS[i]
+    return make_case(2000 + i, 3, 16, 4096, BF16, t, 32,
+                     name=f"decode 3q x 16h bf16, {t:,} tokens, capacity 262,144")
+
+
+def prompt_case() -> Case:
+    return make_case(3000, 256, 16, 2048, BF16, 131_072, 32, active_blocks=2048,
+                     name="prompt 256q x 16h bf16, 131,072 tokens")
+
+
+def deep_case(i: int) -> Case:
+    t = DEEP_TOKENS[i]
+    nb = int(blocks_for_tokens(t))
+    return make_case(4000 + i, 256, 16, 8192, BF16, t, 32, active_blocks=nb,
+                     name=f"deep 256q x 16h bf16, {t:,} tokens, capacity 524,288")
+
+
+def stress_case(kind: str) -> Case:
+    """End-to-end stress cases at 256 queries and 131,072 tokens."""
+    if kind == "equal_kblk":
+        return make_case(5000, 256, 16, 2048, BF16, 131_072, 32, active_blocks=2048,
+                         kblk_equal=True, name="stress: every kblk row identical")
+    if kind == "w_zero":
+        return make_case(5002, 256, 16, 2048, BF16, 131_072, 32, active_blocks=2048,
+                         w_zero=True, name="stress: w = 0")
+    if kind == "ragged":
+        toks = ragged_tokens(5003, 256, 2048)
+        return make_case(5003, 256, 16, 2048, BF16, toks, 32, active_blocks=2048,
+                         name="stress: per-query contexts 1..2,048 blocks, partial tail")
+    raise ValueError(kind)
