@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the block-selection hot path: indexer block scorer + block top-k.
+
+One step = one chained select call (scorer, then top-k) on the deep prompt
+workload: 256 queries x 16 indexer heads x head dim 128, bf16 q and kblk
+~ N(0,1), fp32 w ~ U(0,1), 520,000 tokens of context (8,125 blocks of 64, the
+last one partial), k = 32, KV capacity 524,288 tokens.  Inputs are resident in
+HBM; L2 is flushed (a 256 MB write) before every timed step; each step is
+timed with CUDA events on the launching stream.
+
+Printed (rank 0, one JSON line): the metric (us per select call, lower is
+better), the dominant kernel's roofline against MEASURED_PEAKS.json, the
+top-k and decode-window (3 queries, 258,000 tokens) figures, an end-to-end
+number through the C ABI with host buffers (H2D of the inputs and D2H of the
+ids inside the timed region), SM clocks sampled during the timed region, and
+the CPU oracle timed on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on the host cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_kv_gb300 import inputs  # noqa: E402
+
+METRIC = "us per select call (score+top-k), 256q x 520K tokens"
+UNIT = "us/call"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(case):
+    n = int(case.n_blocks[0])
+    return {
+        "workload": f"deep prompt call: {case.nq} queries x {case.n_heads} heads x 128, bf16, "
+                    f"{int(case.tokens[0]):,} tokens ({n:,} blocks of 64), k={case.k}, capacity 524,288 tokens",
+        "nq": case.nq, "n_heads": case.n_heads, "n_blocks": n, "k": case.k,
+        "l2": "flushed before every timed step (256 MB write)",
+        "path": "chained select (tcgen05 scorer -> top-k auto path)",
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 100 ms while active."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd[1:1] = ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "sparse_attention_kv_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_file)
+    if not e or e.get("source_sha") != kernel_source_hash(kernel_file):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def timed_loop(torch, fn, steps, flush, stream):
+    """Per-step CUDA-event times (ms) of fn(), L2 flushed before each step."""
+    times = []
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    for s, e in zip(starts, ends):
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle on the host cores: each step scores and selects a bounded sample of queries."""
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    case = inputs.deep_case(2)
+    sample_q = args.ref_sample_queries
+    sub = slice(0, sample_q)
+
+    def step():
+        s = oracle.block_scores(case.q[sub], case.w[sub], case.kblk, case.n_blocks[sub], case.dtype)
+        oracle.select(s, case.n_blocks[sub], case.k)
+
+    for _ in range(args.warmup):
+        step()
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        t.append(time.perf_counter() - t0)
+    per_call_us = statistics.mean(t) * 1e6 * case.nq / sample_q
+    cfg = workload_config(case)
+    cfg["path"] = "CPU oracle (FP64 scores, full sort), single thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": per_call_us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(t) * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/kblk, U(0,1) w)", "config": cfg,
+        "cpu_baseline": {"value": per_call_us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{sample_q} of {case.nq} queries per step, scaled to the full call"},
+        "e2e": {"value": per_call_us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def cpu_baseline(case, target_s=10.0):
+    import oracle
+    oracle.build()
+    per_q = []
+    done = 0
+    t_start = time.perf_counter()
+    while done < case.nq and (time.perf_counter() - t_start) < target_s:
+        sl = slice(done, done + 4)
+        t0 = time.perf_counter()
+        s = oracle.block_scores(case.q[sl], case.w[sl], case.kblk, case.n_blocks[sl], case.dtype)
+        oracle.select(s, case.n_blocks[sl], case.k)
+        per_q.append((time.perf_counter() - t0) / len(case.n_blocks[sl]))
+        done += len(case.n_blocks[sl])
+    us = statistics.mean(per_q) * case.nq * 1e6
+    return {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {case.nq} queries of the same workload (about {target_s:.0f} s), "
+                      f"FP64 scores + full sort, single thread, scaled to the full call"}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from sparse_attention_kv_gb300 import qsa
+    from tests import parity
+    qsa.load()
+    stream = torch.cuda.current_stream()
+
+    case = inputs.deep_case(2)
+    q, w, kb, nb = parity.to_device(case, dev)
+    C = case.max_blocks
+    n = int(case.n_blocks[0])
+    scores = torch.empty((case.nq, C), dtype=torch.float32, device=dev)
+    ids = torch.empty((case.nq, case.k), dtype=torch.int32, device=dev)
+    ws = qsa.alloc_workspace(case.nq, C, case.k, device=dev)
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    def select():
+        qsa.select(q, w, kb, nb, case.k, ids, ws, scores=scores, active_blocks=case.active_blocks)
+
+    def score_only():
+        qsa.block_scores(q, w, kb, nb, scores, active_blocks=case.active_blocks, ws=ws)
+
+    def topk_only():
+        qsa.block_topk(scores, nb, case.k, ids, ws, active_blocks=case.active_blocks)
+
+    path = qsa.auto_path(case.nq, C, case.active_blocks, case.k)
+    topk_launches = {qsa.PATH_SAMPLE: 2}.get(path, 1)
+
+    # decode window, 3 queries at 258,000 tokens
+    dcase = inputs.decode_case(5)
+    dq, dw, dkb, dnb = parity.to_device(dcase, dev)
+    dscores = torch.empty((dcase.nq, dcase.max_blocks), dtype=torch.float32, device=dev)
+    dids = torch.empty((dcase.nq, dcase.k), dtype=torch.int32, device=dev)
+    dws = qsa.alloc_workspace(dcase.nq, dcase.max_blocks, dcase.k, device=dev)
+    dpath = qsa.auto_path(dcase.nq, dcase.max_blocks, -1, dcase.k)
+
+    def decode_select():
+        qsa.select(dq, dw, dkb, dnb, dcase.k, dids, dws, scores=dscores, active_blocks=-1)
+
+    # end to end: pinned host inputs -> device, select, ids -> pinned host
+    hq = q.cpu().pin_memory()
+    hw = w.cpu().pin_memory()
+    hkb = kb.cpu().pin_memory()
+    hnb = nb.cpu().pin_memory()
+    hids = torch.empty_like(ids, device="cpu").pin_memory()
+    eq_, ew_, ekb_, enb_ = (torch.empty_like(t) for t in (q, w, kb, nb))
+
+    def e2e_step():
+        eq_.copy_(hq, non_blocking=True)
+        ew_.copy_(hw, non_blocking=True)
+        ekb_.copy_(hkb, non_blocking=True)
+        enb_.copy_(hnb, non_blocking=True)
+        qsa.select(eq_, ew_, ekb_, enb_, case.k, ids, ws, scores=scores, active_blocks=case.active_blocks)
+        hids.copy_(ids, non_blocking=True)
+
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hw, hkb, hnb))
+    d2h = hids.numel() * hids.element_size()
+
+    # warm-up (also brings the clocks up)
+    for _ in range(max(3, args.warmup)):
+        flush()
+        select()
+        decode_select()
+        e2e_step()
+    torch.cuda.synchronize()
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        select()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_uuid}" if gpu_uuid and not str(gpu_uuid).startswith("GPU-") else (
+        str(gpu_uuid) if gpu_uuid else None)
+    sampler = ClockSampler(gpu_id).start()
+    time.sleep(0.25)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_main = timed_loop(torch, select, args.steps, flush, stream)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    reps = max(args.steps, 200)
+    t_score = timed_loop(torch, score_only, reps, flush, stream)
+    t_topk = timed_loop(torch, topk_only, reps, flush, stream)
+    t_dec = timed_loop(torch, decode_select, reps, flush, stream)
+    t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream)
+    clocks = sampler.stop()
+
+    ms_main = statistics.mean(t_main)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_main], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_main = float(tt.item())
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    us_main = ms_main * 1e3 / world          # whole job: world calls per step
+    us_score = statistics.median(t_score) * 1e3
+    us_topk = statistics.median(t_topk) * 1e3
+    flops = 2.0 * case.nq * case.n_heads * 128 * n
+    topk_bytes = 4.0 * case.nq * n + 4.0 * case.nq * case.k + 4.0 * case.nq
+    tflops = flops / (us_score * 1e-6) / 1e12
+    gbs = topk_bytes / (us_topk * 1e-6) / 1e9
+    if us_score >= us_topk:
+        roof = {"kernel": "scorer_tc_kernel", "bound": "tensor", "achieved": tflops,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                "traffic": profiled_traffic("scorer_tc.cu"),
+                "per_launch": f"{flops:.4g} FLOP (2 x 256 q x 16 h x 128 x {n} blocks)",
+                "us_per_launch": us_score, "peak_source": f"{peak_src} bf16 burst (dense cuBLAS)"}
+    else:
+        roof = {"kernel": "topk", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": profiled_traffic("topk.cu"),
+                "per_launch": f"{topk_bytes:.4g} B", "us_per_launch": us_topk,
+                "peak_source": f"{peak_src} HBM copy"}
+    dec_n = int(dcase.n_blocks[0])
+    dec_bytes = 256.0 * dec_n + 4096.0 * dcase.nq + 64.0 * dcase.nq + 8.0 * dcase.nq * dec_n + 4.0 * dcase.nq * dcase.k
+    us_dec = statistics.median(t_dec) * 1e3
+    us_e2e = statistics.mean(t_e2e) * 1e3
+    line = {
+        "metric": METRIC, "value": us_main, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_main, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/kblk, U(0,1) w)",
+        "config": workload_config(case),
+        "selections_per_s": case.nq * world / (ms_main * 1e-3),
+        "roofline": roof,
+        "scorer": {"us": us_score, "tflops": tflops, "frac_of_bf16_peak": tflops / peaks["bf16_tflops"]},
+        "topk": {"us": us_topk, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                 "path": qsa.PATH_NAMES[path], "bytes": topk_bytes, "l2": "cold (flushed)"},
+        "decode_3q_258K": {"us_per_call": us_dec, "path": qsa.PATH_NAMES[dpath],
+                           "gbs": dec_bytes / (us_dec * 1e-6) / 1e9,
+                           "frac_of_hbm": dec_bytes / (us_dec * 1e-6) / 1e9 / peaks["hbm_gbs"]},
+        "e2e": {"value": us_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + topk_launches),
+        "clocks": clocks,
+        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"]},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-sample-queries", type=int, default=2)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * qsa.h -- C ABI of the GB300 (sm_103a) query-sparse-attention block selection
+ * library, libqsa.so.
+ *
+ * The path selects, for every query, the KV blocks (64 tokens each) that a
+ * sparse attention step will read:
+ *
+ *   1. block scorer:  score[q][b] = sum_h w[q][h] * relu(dot(q[q][h][:], kblk[b][:]))
+ *      over the indexer heads h, head dim 128, one key row per block (the last,
+ *      partial block of a context has a key like any other);
+ *   2. block top-k:   the k blocks of highest score, ties to the lower block id,
+ *      emitted as ids in ascending block order, -1 padded when n < k.
+ *
+ * Sources: the scorer is the "qsa_block_scores" step of "#1091 qsa_select:
+ * FP32 tiled block scores below sm_80" (section "What": rows = query x indexer
+ * head, K = 128, ReLU per head summed per block; the tail block).  The top-k
+ * rule is the threshold / "above" / tie-budget rule of "#2093 sm_75: the
+ * prompt path's top-k with one full read of the scores" (description, steps
+ * 1-4), and the decode split is the two-stage split of Strata PR #3987
+ * (section "Approach").
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument except the ones marked "host" is DEVICE memory owned
+ *    by the caller.  The library never allocates or frees memory on a call, never
+ *    synchronises the device, and keeps no global mutable device state: all
+ *    scratch lives in the caller's workspace.
+ *  - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
+ *    and runs asynchronously; the return value reports host-side validation and
+ *    launch errors only.  Device-side contract violations are recorded as bits in
+ *    the workspace flags word (QSA_FLAG_*), readable with qsa_read_flags().
+ *  - On any error status nothing is enqueued; qsa_last_error() (thread-local)
+ *    returns a one-line reason.
+ *  - One workspace must not be used by two calls that can run concurrently
+ *    (e.g. on two streams); give each stream its own workspace.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_VERSION 1
+
+/* Head dimension of q and kblk rows; the only value supported. */
+#define QSA_HEAD_DIM 128
+/* Largest k (blocks selected per query). */
+#define QSA_MAX_K 1024
+/* Largest max_blocks (KV capacity in blocks). */
+#define QSA_MAX_BLOCKS (1 << 24)
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or enum value */
+    QSA_ERR_UNSUPPORTED = 2, /* a forced path that cannot run this shape */
+    QSA_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than qsa_workspace_bytes() */
+    QSA_ERR_CUDA = 4         /* a CUDA runtime/driver call or a launch failed */
+} qsa_status;
+
+typedef enum {
+    QSA_F32 = 0,  /* IEEE binary32 */
+    QSA_BF16 = 1  /* bfloat16 (upper half of a binary32) */
+} qsa_dtype;
+
+/* Top-k path.  AUTO picks from host-visible sizes only; the others force a path
+ * (tests).  Every path returns the same ids. */
+typedef enum {
+    QSA_PATH_AUTO = 0,
+    QSA_PATH_SPLIT = 1,    /* multi-CTA chunk split + last-CTA merge (decode windows) */
+    QSA_PATH_SAMPLE = 2,   /* one read against a sampled lower bound (+ radix fallback) */
+    QSA_PATH_REGISTER = 3, /* whole row in registers, one CTA per query */
+    QSA_PATH_RADIX = 4     /* multi-pass radix select over global memory, any size */
+} qsa_path;
+
+typedef void *qsa_stream; /* a cudaStream_t */
+
+/* Bits of the workspace flags word (sticky until cleared by qsa_read_flags). */
+#define QSA_FLAG_NBLOCKS_CLAMPED 0x1u /* some n_blocks[q] was < 0 or > its bound; clamped */
+#define QSA_FLAG_WAIT_TIMEOUT 0x2u    /* a kernel gave up a bounded wait; its outputs are invalid */
+#define QSA_FLAG_INTERNAL 0x4u        /* an internal consistency check failed */
+
+/*
+ * Workspace size in bytes for calls with these sizes (any path, fused or not).
+ * A workspace sized for (nq, max_blocks, k) serves every call with sizes at or
+ * below these.  The workspace must be zero-filled before its first use (e.g. by
+ * qsa_workspace_init); every call leaves it in a reusable state.  Returns 0 for
+ * invalid sizes.
+ */
+size_t qsa_workspace_bytes(int nq, int max_blocks, int k, int fused);
+
+/* Zero-fill `ws_bytes` bytes of workspace `ws` on `stream` (cudaMemsetAsync). */
+qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
+
+/*
+ * Block scores: scores[q * scores_stride + b] for 0 <= b < n_blocks[q].
+ *
+ *   q        [nq][n_heads][128]  dtype `dt` (fp32 or bf16), row-major, 16-byte aligned
+ *   w        [nq][n_heads]       fp32
+ *   kblk     [max_blocks][128]   dtype `dt`, row-major, 16-byte aligned
+ *   n_blocks [nq]                int32 on the DEVICE: blocks in each query's context,
+ *                                clamped on the device to [0, bound] where bound =
+ *                                active_blocks if active_blocks >= 0, else max_blocks
+ *                                (a clamp sets QSA_FLAG_NBLOCKS_CLAMPED)
+ *   active_blocks                host int: -1 (unknown) or an upper bound on every
+ *                                n_blocks[q] (values above max_blocks act as max_blocks);
+ *                                it sizes the grid and never changes a result
+ *   scores   [nq][scores_stride] fp32, scores_stride >= max_blocks; entries at
+ *                                b >= n_blocks[q] are not written
+ *   ws, ws_bytes                 workspace (may be NULL/0: then device flags are not
+ *                                recorded)
+ *
+ * Arithmetic: products on the tensor cores (bf16 x bf16 -> fp32, or fp32 split in
+ * three tf32 products), accumulated in fp32; ReLU and the head-weighted sum in
+ * fp32.  n_heads must be 1, 2, 4, 8 or 16.
+ * Errors: QSA_ERR_INVALID_ARG for NULL q/w/kblk/n_blocks/scores, nq < 1,
+ * head_dim != 128, unsupported n_heads, max_blocks outside [1, QSA_MAX_BLOCKS],
+ * scores_stride < max_blocks, misaligned q/kblk, bad dtype.
+ */
+qsa_status qsa_block_scores(const void *q, const float *w, const void *kblk, qsa_dtype dt,
+                            const int32_t *n_blocks, int nq, int n_heads, int head_dim,
+                            int max_blocks, int active_blocks, float *scores,
+                            int64_t scores_stride, void *ws, size_t ws_bytes, qsa_stream stream);
+
+/*
+ * Block top-k over given fp32 scores.
+ *
+ *   scores   [nq][scores_stride] fp32 (NaN is outside the contract; -0 == +0)
+ *   n_blocks [nq] int32 on the DEVICE, clamped as for qsa_block_scores
+ *   k        1 <= k <= QSA_MAX_K
+ *   ids      [nq][k] int32 out: the selected block ids in ascending order; when
+ *            n_blocks[q] < k the first n_blocks[q] slots hold 0..n-1 and the rest -1
+ *   ws       workspace of at least qsa_workspace_bytes(nq, max_blocks, k, 0) bytes
+ *   path     QSA_PATH_AUTO, or a forced path (QSA_ERR_UNSUPPORTED if it cannot run
+ *            this shape)
+ *
+ * Selection: keep the blocks that come first in the order (score descending,
+ * block id ascending).  Every path gives the same ids.
+ */
+qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int32_t *n_blocks,
+                          int nq, int max_blocks, int active_blocks, int k, int32_t *ids,
+                          void *ws, size_t ws_bytes, qsa_path path, qsa_stream stream);
+
+/*
+ * Score then select, in one call.
+ *
+ * fused == 0 (chained): the scorer writes `scores` (required), then the top-k
+ *   reads them; both are the calls above.
+ * fused != 0: the scorer's epilogue keeps each CTA's block range on chip, picks
+ *   that range's candidates and the last CTA of a query group merges them; the
+ *   scores never go to HBM.  `scores` may be NULL; when given, it also receives
+ *   the scores (bit-identical to the chained scorer's).
+ * Arguments as in qsa_block_scores / qsa_block_topk; ws must hold
+ * qsa_workspace_bytes(nq, max_blocks, k, fused) bytes.
+ */
+qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype dt,
+                      const int32_t *n_blocks, int nq, int n_heads, int head_dim, int max_blocks,
+                      int active_blocks, int k, int32_t *ids, float *scores,
+                      int64_t scores_stride, int fused, void *ws, size_t ws_bytes,
+                      qsa_path path, qsa_stream stream);
+
+/*
+ * Copy the workspace flags word (QSA_FLAG_* bits) to host `*flags`, waiting for
+ * `stream` to finish; clear it on the device when `clear` is nonzero.
+ */
+qsa_status qsa_read_flags(void *ws, uint32_t *flags /* host */, int clear, qsa_stream stream);
+
+/* The path QSA_PATH_AUTO takes for these host-visible sizes (no launch). */
+qsa_path qsa_auto_path(int nq, int max_blocks, int active_blocks, int k);
+
+/* One-line reason for the last error status returned on this thread. */
+const char *qsa_last_error(void);
+
+/* QSA_VERSION of the loaded library. */
+int qsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

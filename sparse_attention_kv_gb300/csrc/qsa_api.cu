@@ -1,0 +1,273 @@
+// qsa_api.cu -- the C ABI of libqsa.so: argument checks, workspace layout,
+// top-k path dispatch, and the chained select.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "qsa_internal.h"
+
+namespace qsa {
+
+static thread_local char g_err[512] = "";
+
+qsa_status fail(qsa_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qsa_status check_cuda(cudaError_t err, const char *what) {
+    if (err == cudaSuccess) return QSA_OK;
+    return fail(QSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+int num_sms() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int nq, int max_blocks, int k) {
+    WsLayout L{};
+    L.maxch = (max_blocks + kMinChunk - 1) / kMinChunk;
+    size_t off = 0;
+    L.flags = off;
+    off += 256;
+    L.tickets = off;
+    off += align256(sizeof(uint32_t) * (size_t)nq);
+    L.qflags = off;
+    off += align256(sizeof(uint32_t) * (size_t)nq);
+    L.counts = off;
+    off += align256(sizeof(int32_t) * (size_t)nq * L.maxch);
+    L.ckeys = off;
+    off += align256(sizeof(uint32_t) * (size_t)nq * L.maxch * k);
+    L.cids = off;
+    off += align256(sizeof(int32_t) * (size_t)nq * L.maxch * k);
+    L.total = off;
+    return L;
+}
+
+static int effective_bound(int max_blocks, int active_blocks) {
+    return active_blocks >= 0 ? (active_blocks < max_blocks ? active_blocks : max_blocks) : max_blocks;
+}
+
+// Prompt calls above this many active blocks take the sampled filter; below it the
+// register path reads the row once too and has no sampling step.
+static constexpr int kSampleMinBlocks = 2048;
+
+static qsa_path auto_path(int nq, int max_blocks, int active_blocks, int k) {
+    const int bound = effective_bound(max_blocks, active_blocks);
+    const WsLayout L = ws_layout(nq, max_blocks, k);
+    if (active_blocks < 0 && nq <= 16 && bound > k && split_geometry(bound, nq, k, L.maxch).chunk_len > 0)
+        return QSA_PATH_SPLIT;
+    if (bound <= kRegisterCap) {
+        if (active_blocks >= 0 && bound >= kSampleMinBlocks) return QSA_PATH_SAMPLE;
+        return QSA_PATH_REGISTER;
+    }
+    return QSA_PATH_RADIX;
+}
+
+static qsa_status check_common(int nq, int max_blocks, int active_blocks) {
+    if (nq < 1) return fail(QSA_ERR_INVALID_ARG, "nq must be >= 1 (got %d)", nq);
+    if (max_blocks < 1 || max_blocks > QSA_MAX_BLOCKS)
+        return fail(QSA_ERR_INVALID_ARG, "max_blocks must be in [1, %d] (got %d)", QSA_MAX_BLOCKS,
+                    max_blocks);
+    if (active_blocks < -1)
+        return fail(QSA_ERR_INVALID_ARG, "active_blocks must be -1 or >= 0 (got %d)", active_blocks);
+    return QSA_OK;
+}
+
+static qsa_status check_ws(void *ws, size_t ws_bytes, int nq, int max_blocks, int k) {
+    if (!ws) return fail(QSA_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return fail(QSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    const size_t need = ws_layout(nq, max_blocks, k).total;
+    if (ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
+    return QSA_OK;
+}
+
+static qsa_status check_scorer_args(const void *q, const float *w, const void *kblk, int dt,
+                                    const int32_t *n_blocks, int nq, int n_heads, int head_dim,
+                                    int max_blocks, int active_blocks, const float *scores,
+                                    int64_t stride, bool scores_required) {
+    qsa_status st = check_common(nq, max_blocks, active_blocks);
+    if (st != QSA_OK) return st;
+    if (!q || !w || !kblk || !n_blocks) return fail(QSA_ERR_INVALID_ARG, "NULL q, w, kblk or n_blocks");
+    if (scores_required && !scores) return fail(QSA_ERR_INVALID_ARG, "scores is NULL");
+    if (dt != QSA_F32 && dt != QSA_BF16) return fail(QSA_ERR_INVALID_ARG, "bad dtype %d", dt);
+    if (head_dim != QSA_HEAD_DIM)
+        return fail(QSA_ERR_INVALID_ARG, "head_dim must be %d (got %d)", QSA_HEAD_DIM, head_dim);
+    if (n_heads != 1 && n_heads != 2 && n_heads != 4 && n_heads != 8 && n_heads != 16)
+        return fail(QSA_ERR_INVALID_ARG, "n_heads must be 1, 2, 4, 8 or 16 (got %d)", n_heads);
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kblk)) & 15u)
+        return fail(QSA_ERR_INVALID_ARG, "q and kblk must be 16-byte aligned");
+    if (scores && stride < max_blocks)
+        return fail(QSA_ERR_INVALID_ARG, "scores_stride %lld < max_blocks %d", (long long)stride,
+                    max_blocks);
+    if ((long long)nq * n_heads > (1ll << 30)) return fail(QSA_ERR_INVALID_ARG, "nq * n_heads too large");
+    return QSA_OK;
+}
+
+static TopkArgs make_topk_args(const float *scores, int64_t stride, const int32_t *n_blocks, int nq,
+                               int bound, int k, int32_t *ids, void *ws, const WsLayout &L) {
+    char *base = static_cast<char *>(ws);
+    TopkArgs a{};
+    a.scores = scores;
+    a.stride = stride;
+    a.n_blocks = n_blocks;
+    a.nq = nq;
+    a.bound = bound;
+    a.k = k;
+    a.ids = ids;
+    a.flags = reinterpret_cast<uint32_t *>(base + L.flags);
+    a.tickets = reinterpret_cast<uint32_t *>(base + L.tickets);
+    a.qflags = reinterpret_cast<uint32_t *>(base + L.qflags);
+    a.counts = reinterpret_cast<int32_t *>(base + L.counts);
+    a.ckeys = reinterpret_cast<uint32_t *>(base + L.ckeys);
+    a.cids = reinterpret_cast<int32_t *>(base + L.cids);
+    a.maxch = L.maxch;
+    return a;
+}
+
+static qsa_status run_topk(const float *scores, int64_t stride, const int32_t *n_blocks, int nq,
+                           int max_blocks, int active_blocks, int k, int32_t *ids, void *ws,
+                           qsa_path path, cudaStream_t s) {
+    const int bound = effective_bound(max_blocks, active_blocks);
+    const WsLayout L = ws_layout(nq, max_blocks, k);
+    const TopkArgs a = make_topk_args(scores, stride, n_blocks, nq, bound, k, ids, ws, L);
+    if (path == QSA_PATH_AUTO) path = auto_path(nq, max_blocks, active_blocks, k);
+    switch (path) {
+    case QSA_PATH_SPLIT: {
+        const SplitGeom g = split_geometry(bound, nq, k, L.maxch);
+        return launch_topk_split(a, g, s);
+    }
+    case QSA_PATH_SAMPLE:
+        if (bound > kRegisterCap)
+            return fail(QSA_ERR_UNSUPPORTED, "sample path holds at most %d blocks per row (bound %d)",
+                        kRegisterCap, bound);
+        return launch_topk_sample(a, s);
+    case QSA_PATH_REGISTER:
+        return launch_topk_register(a, s);
+    case QSA_PATH_RADIX:
+        return launch_topk_radix(a, false, s);
+    default:
+        return fail(QSA_ERR_INVALID_ARG, "bad path %d", (int)path);
+    }
+}
+
+}  // namespace qsa
+
+using namespace qsa;
+
+extern "C" {
+
+size_t qsa_workspace_bytes(int nq, int max_blocks, int k, int fused) {
+    (void)fused;
+    if (nq < 1 || max_blocks < 1 || max_blocks > QSA_MAX_BLOCKS || k < 1 || k > QSA_MAX_K) return 0;
+    return ws_layout(nq, max_blocks, k).total;
+}
+
+qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream) {
+    if (!ws) return fail(QSA_ERR_WORKSPACE, "workspace is NULL");
+    return check_cuda(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)),
+                      "cudaMemsetAsync(workspace)");
+}
+
+qsa_status qsa_block_scores(const void *q, const float *w, const void *kblk, qsa_dtype dt,
+                            const int32_t *n_blocks, int nq, int n_heads, int head_dim,
+                            int max_blocks, int active_blocks, float *scores,
+                            int64_t scores_stride, void *ws, size_t ws_bytes, qsa_stream stream) {
+    qsa_status st = check_scorer_args(q, w, kblk, (int)dt, n_blocks, nq, n_heads, head_dim,
+                                      max_blocks, active_blocks, scores, scores_stride, true);
+    if (st != QSA_OK) return st;
+    if (ws && ws_bytes < 256) return fail(QSA_ERR_WORKSPACE, "workspace smaller than its 256-byte header");
+    ScorerArgs a{};
+    a.q = q;
+    a.w = w;
+    a.kblk = kblk;
+    a.dt = dt;
+    a.n_blocks = n_blocks;
+    a.nq = nq;
+    a.n_heads = n_heads;
+    a.max_blocks = max_blocks;
+    a.bound = effective_bound(max_blocks, active_blocks);
+    a.scores = scores;
+    a.stride = scores_stride;
+    a.flags = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + ws_layout(nq, max_blocks, 1).flags)
+                 : nullptr;
+    return launch_scorer(a, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int32_t *n_blocks,
+                          int nq, int max_blocks, int active_blocks, int k, int32_t *ids,
+                          void *ws, size_t ws_bytes, qsa_path path, qsa_stream stream) {
+    qsa_status st = check_common(nq, max_blocks, active_blocks);
+    if (st != QSA_OK) return st;
+    if (!scores || !n_blocks || !ids) return fail(QSA_ERR_INVALID_ARG, "NULL scores, n_blocks or ids");
+    if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
+    if (scores_stride < max_blocks)
+        return fail(QSA_ERR_INVALID_ARG, "scores_stride %lld < max_blocks %d", (long long)scores_stride,
+                    max_blocks);
+    st = check_ws(ws, ws_bytes, nq, max_blocks, k);
+    if (st != QSA_OK) return st;
+    return run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ids, ws, path,
+                    static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype dt,
+                      const int32_t *n_blocks, int nq, int n_heads, int head_dim, int max_blocks,
+                      int active_blocks, int k, int32_t *ids, float *scores,
+                      int64_t scores_stride, int fused, void *ws, size_t ws_bytes,
+                      qsa_path path, qsa_stream stream) {
+    qsa_status st = check_scorer_args(q, w, kblk, (int)dt, n_blocks, nq, n_heads, head_dim,
+                                      max_blocks, active_blocks, scores, scores_stride, !fused);
+    if (st != QSA_OK) return st;
+    if (!ids) return fail(QSA_ERR_INVALID_ARG, "ids is NULL");
+    if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
+    st = check_ws(ws, ws_bytes, nq, max_blocks, k);
+    if (st != QSA_OK) return st;
+    if (fused) return fail(QSA_ERR_UNSUPPORTED, "fused score-then-select is not built yet");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = qsa_block_scores(q, w, kblk, dt, n_blocks, nq, n_heads, head_dim, max_blocks, active_blocks,
+                          scores, scores_stride, ws, ws_bytes, stream);
+    if (st != QSA_OK) return st;
+    return run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ids, ws, path, s);
+}
+
+qsa_status qsa_read_flags(void *ws, uint32_t *flags, int clear, qsa_stream stream) {
+    if (!ws || !flags) return fail(QSA_ERR_INVALID_ARG, "NULL workspace or flags");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    qsa_status st = check_cuda(cudaMemcpyAsync(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, s),
+                               "cudaMemcpyAsync(flags)");
+    if (st != QSA_OK) return st;
+    st = check_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (st != QSA_OK) return st;
+    if (clear) return check_cuda(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s), "cudaMemsetAsync(flags)");
+    return QSA_OK;
+}
+
+qsa_path qsa_auto_path(int nq, int max_blocks, int active_blocks, int k) {
+    if (nq < 1 || max_blocks < 1 || k < 1) return QSA_PATH_AUTO;
+    return auto_path(nq, max_blocks, active_blocks, k);
+}
+
+const char *qsa_last_error(void) { return g_err; }
+
+int qsa_version(void) { return QSA_VERSION; }
+
+}  // extern "C"

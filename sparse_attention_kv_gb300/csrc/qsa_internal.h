@@ -1,0 +1,89 @@
+// qsa_internal.h -- host-side declarations shared by the translation units of
+// libqsa.so (launchers, workspace layout, error reporting).  Not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+// Record a one-line reason for the status about to be returned (thread-local).
+qsa_status fail(qsa_status st, const char *fmt, ...);
+// Map a CUDA error to QSA_ERR_CUDA with a reason; QSA_OK when err == cudaSuccess.
+qsa_status check_cuda(cudaError_t err, const char *what);
+
+int num_sms();  // SM count of the current device (cached per device)
+
+// Candidate slots per (query, chunk) are sized for chunks of at least this many blocks.
+constexpr int kMinChunk = 128;
+// Shared-memory candidate capacity of the sampled-bound filter.
+constexpr int kSampleCap = 4096;
+// Largest row the register and sample paths hold on chip (1024 threads x 8 keys).
+constexpr int kRegisterCap = 8192;
+// Stage-B capacity of the split (slots of nchunks x k held by 256 threads x 16).
+constexpr int kSplitSlots = 4096;
+// Largest chunk of the split's stage A (256 threads x 4 keys).
+constexpr int kSplitMaxChunk = 1024;
+
+// Workspace layout; every region starts on a 256-byte boundary.
+struct WsLayout {
+    size_t flags;     // uint32 flags word (QSA_FLAG_*)
+    size_t tickets;   // uint32 [nq]       last-CTA tickets (zero between calls)
+    size_t qflags;    // uint32 [nq]       per-query fallback flags of the sampled filter
+    size_t counts;    // int32  [nq][maxch] candidates per chunk
+    size_t ckeys;     // uint32 [nq][maxch][k]
+    size_t cids;      // int32  [nq][maxch][k]
+    size_t total;
+    int maxch;
+};
+WsLayout ws_layout(int nq, int max_blocks, int k);
+
+struct TopkArgs {
+    const float *scores;
+    int64_t stride;
+    const int32_t *n_blocks;
+    int nq;
+    int bound;   // clamp bound of n_blocks (active blocks or capacity)
+    int k;
+    int32_t *ids;
+    uint32_t *flags;
+    uint32_t *tickets;
+    uint32_t *qflags;
+    int32_t *counts;
+    uint32_t *ckeys;
+    int32_t *cids;
+    int maxch;
+};
+
+// Split geometry for a bound; chunk_len == 0 when the split cannot take it.
+struct SplitGeom {
+    int chunk_len;
+    int nchunks;
+};
+SplitGeom split_geometry(int bound, int nq, int k, int maxch);
+
+qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s);
+qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s);
+qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s);
+qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s);
+
+struct ScorerArgs {
+    const void *q;
+    const float *w;
+    const void *kblk;
+    qsa_dtype dt;
+    const int32_t *n_blocks;
+    int nq;
+    int n_heads;
+    int max_blocks;
+    int bound;
+    float *scores;
+    int64_t stride;
+    uint32_t *flags;
+};
+qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);
+
+}  // namespace qsa

@@ -1,0 +1,555 @@
+// scorer_tc.cu -- indexer block scorer on the 5th-generation tensor cores.
+//
+//   score[q][b] = sum_h w[q][h] * relu(dot(q[q][h][:], kblk[b][:]))
+//
+// The contraction is the GEMM of "#1091 qsa_select: FP32 tiled block scores
+// below sm_80" (section "What": rows = query x indexer head, K = 128, the ReLU
+// of each head summed per block), laid out for tcgen05: the MMA's M side is 128
+// KV blocks (one TMEM lane each), its N side is a group of queries x heads
+// (<= 256 columns), K = 128.  One thread of the epilogue owns one block row of
+// the accumulator, so the ReLU and the head-weighted sum stay in its registers
+// and the score stores of a warp are 32 consecutive blocks.
+//
+// Per CTA (192 threads): warp 0 issues TMA loads (kblk tiles through a ring of
+// shared-memory stages, the query-group tile once), warp 1 owns TMEM and issues
+// tcgen05.mma from one thread, warps 2-5 drain the double-buffered accumulator
+// (tcgen05.ld) and write the scores.  bf16 inputs use kind::f16 (bf16 x bf16 ->
+// fp32).  fp32 inputs use kind::tf32 on a three-term split a = a_hi + a_lo
+// (a_hi = a with the low 13 mantissa bits cleared): a_hi*b_hi + a_hi*b_lo +
+// a_lo*b_hi, which keeps the product error near 2^-20 relative.
+//
+// The partial tail block of a context is a key row like any other; rows at or
+// past n_blocks[q] are computed but not stored, rows past the capacity are
+// zero-filled by TMA.  Every wait on an mbarrier is bounded; on expiry the CTA
+// raises QSA_FLAG_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kBM = 128;       // KV blocks per tile (MMA M = TMEM lanes)
+constexpr int kThreads = 192;  // 6 warps
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
+
+template <bool F32>
+struct Cfg;
+template <>
+struct Cfg<false> {  // bf16 -> kind::f16
+    static constexpr int kEsize = 2, kEPA = 64, kAtoms = 2, kStages = 4, kMaxBN = 256;
+    static constexpr uint32_t kFmt = 1;
+};
+template <>
+struct Cfg<true> {  // fp32 -> kind::tf32, three-term split
+    static constexpr int kEsize = 4, kEPA = 32, kAtoms = 4, kStages = 1, kMaxBN = 64;
+    static constexpr uint32_t kFmt = 2;
+};
+
+// One 128-byte swizzle atom of a tile holds rows x 128 bytes (kEPA elements of K).
+constexpr int kAtomA = kBM * 128;  // 16 KB
+
+template <bool F32>
+struct Layout {
+    using C = Cfg<F32>;
+    static constexpr int kB = C::kAtoms * C::kMaxBN * 128;
+    static constexpr int kAStage = C::kAtoms * kAtomA;
+    static constexpr int offB = 0;
+    static constexpr int offBlo = offB + kB;
+    static constexpr int offA = offBlo + (F32 ? kB : 0);
+    static constexpr int offAlo = offA + C::kStages * kAStage;
+    static constexpr int offCtrl = offAlo + (F32 ? C::kStages * kAStage : 0);
+};
+
+struct Ctrl {
+    uint64_t full[4], empty[4], split[4];
+    uint64_t bfull, bsplit, done;
+    uint64_t tfull[2], tempty[2];
+    uint32_t tmem_base;
+    int abort;
+    int maxn;
+    int pad;
+    float w[256];
+    int nb[256];
+};
+
+template <bool F32>
+constexpr int smem_bytes() { return Layout<F32>::offCtrl + (int)sizeof(Ctrl) + 1024; }
+
+struct KParams {
+    const float *w;
+    const int32_t *n_blocks;
+    float *scores;
+    int64_t stride;
+    uint32_t *flags;
+    int nq, bound, qg, bn, tiles_per_cta, tmem_cols;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete.  Gives up when another
+// thread has aborted or after kWaitNs (then raises the abort itself).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (now_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// Bounded wait that never raises the abort (used while draining).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const unsigned long long t0 = now_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (now_ns() - t0 > kWaitNs) return;
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+template <bool F32>
+__device__ __forceinline__ void mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    if constexpr (F32) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+            : "memory");
+    }
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (SBO); the leading offset is unused for this layout.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor: fp32 accumulator, A/B format `fmt`, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc(uint32_t fmt, int M, int N) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// a = hi + lo with hi = a truncated to tf32 (exact split), in place for hi.
+__device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes, int tid, int nthreads) {
+    uint4 *p = reinterpret_cast<uint4 *>(buf);
+    uint4 *l = reinterpret_cast<uint4 *>(lo);
+    for (int i = tid; i < bytes / 16; i += nthreads) {
+        uint4 x = p[i], h, r;
+        h.x = x.x & 0xFFFFE000u;
+        h.y = x.y & 0xFFFFE000u;
+        h.z = x.z & 0xFFFFE000u;
+        h.w = x.w & 0xFFFFE000u;
+        r.x = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(h.x));
+        r.y = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(h.y));
+        r.z = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(h.z));
+        r.w = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(h.w));
+        p[i] = h;
+        l[i] = r;
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <bool F32, int H>
+__global__ void __launch_bounds__(kThreads, 1)
+    scorer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                     const KParams p) {
+    using C = Cfg<F32>;
+    using L = Layout<F32>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sB = smem + L::offB;
+    uint8_t *sBlo = smem + L::offBlo;
+    uint8_t *sA = smem + L::offA;
+    uint8_t *sAlo = smem + L::offAlo;
+    Ctrl &ct = *reinterpret_cast<Ctrl *>(smem + L::offCtrl);
+    volatile int *abort_flag = &ct.abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.y;
+    const int q0 = g * p.qg;
+    const int qv = min(p.qg, p.nq - q0);  // queries of this group
+    const int bn = p.bn;
+
+    for (int i = tid; i < qv * H; i += kThreads) ct.w[i] = p.w[(size_t)q0 * H + i];
+    if (warp == 0) {
+        int mx = 0;
+        for (int j = lane; j < qv; j += 32) {
+            int n = p.n_blocks[q0 + j];
+            if (n < 0 || n > p.bound) {
+                if (p.flags && blockIdx.x == 0) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
+                n = n < 0 ? 0 : p.bound;
+            }
+            ct.nb[j] = n;
+            mx = max(mx, n);
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) ct.maxn = mx;
+    }
+    if (tid == 32) {
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&ct.full[s], 1);
+            mbar_init(&ct.empty[s], 1);
+            mbar_init(&ct.split[s], 128);
+        }
+        mbar_init(&ct.bfull, 1);
+        mbar_init(&ct.bsplit, 128);
+        mbar_init(&ct.done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ct.tfull[b], 1);
+            mbar_init(&ct.tempty[b], 128);
+        }
+        ct.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int ntiles_g = (ct.maxn + kBM - 1) / kBM;
+    const int t_begin = blockIdx.x * p.tiles_per_cta;
+    const int ntiles = min(t_begin + p.tiles_per_cta, ntiles_g) - t_begin;
+    if (ntiles <= 0) return;
+
+    if (warp == 1) {
+        tmem_alloc(&ct.tmem_base, (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ct.tmem_base;
+    const int buf_cols = p.tmem_cols / 2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+            mbar_expect_tx(&ct.bfull, (uint32_t)(C::kAtoms * bn * 128));
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_2d(sB + a * bn * 128, &tm_q, &ct.bfull, a * C::kEPA, q0 * H);
+            int issued = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % C::kStages;
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                if (!mbar_wait(&ct.empty[s], ph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(&ct.full[s], (uint32_t)(C::kAtoms * kAtomA));
+                const int row = (t_begin + i) * kBM;
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_2d(sA + s * L::kAStage + a * kAtomA, &tm_k, &ct.full[s], a * C::kEPA, row);
+                ++issued;
+            }
+            // drain: the latest load of every stage and the query tile
+            for (int j = max(0, issued - C::kStages); j < issued; ++j)
+                mbar_drain(&ct.full[j % C::kStages], (uint32_t)(j / C::kStages) & 1u);
+            mbar_drain(&ct.bfull, 0);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t id = idesc(C::kFmt, kBM, bn);
+            bool ok = mbar_wait(F32 ? &ct.bsplit : &ct.bfull, 0, abort_flag);
+            tc_fence_after();
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int s = i % C::kStages;
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                const int b = i & 1;
+                const uint32_t tph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(&ct.tempty[b], tph ^ 1u, abort_flag)) break;
+                if (!mbar_wait(F32 ? &ct.split[s] : &ct.full[s], ph, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * buf_cols);
+                const uint32_t a0 = smem_u32(sA + s * L::kAStage);
+                const uint32_t al0 = smem_u32(sAlo + s * L::kAStage);
+                const uint32_t b0 = smem_u32(sB);
+                const uint32_t bl0 = smem_u32(sBlo);
+#pragma unroll
+                for (int a = 0; a < C::kAtoms; ++a) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t aoff = (uint32_t)(a * kAtomA + kk * 32);
+                        const uint32_t boff = (uint32_t)(a * bn * 128 + kk * 32);
+                        const uint32_t acc = (a | kk) != 0 ? 1u : 0u;
+                        mma<F32>(d, sdesc(a0 + aoff), sdesc(b0 + boff), id, acc);
+                        if constexpr (F32) {
+                            mma<F32>(d, sdesc(a0 + aoff), sdesc(bl0 + boff), id, 1u);
+                            mma<F32>(d, sdesc(al0 + aoff), sdesc(b0 + boff), id, 1u);
+                        }
+                    }
+                }
+                mma_commit(&ct.empty[s]);
+                mma_commit(&ct.tfull[b]);
+            }
+            // every MMA issued so far has completed once this arrives
+            mma_commit(&ct.done);
+            mbar_drain(&ct.done, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, one accumulator row per thread
+        const int et = tid - 64;                 // 0..127
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        bool ok = true;
+        if constexpr (F32) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&ct.bfull, 0, abort_flag));
+            if (ok) split_tf32(sB, sBlo, C::kAtoms * bn * 128, et, 128);
+            fence_proxy_async();
+            mbar_arrive(&ct.bsplit);
+        }
+        for (int i = 0; ok && i < ntiles; ++i) {
+            if constexpr (F32) {
+                const int s = i % C::kStages;
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&ct.full[s], ph, abort_flag))) break;
+                split_tf32(sA + s * L::kAStage, sAlo + s * L::kAStage, L::kAStage, et, 128);
+                fence_proxy_async();
+                mbar_arrive(&ct.split[s]);
+            }
+            const int b = i & 1;
+            const uint32_t tph = (uint32_t)(i >> 1) & 1u;
+            // warp-uniform: tcgen05.ld below is a warp-collective instruction
+            if (!__all_sync(0xffffffffu, mbar_wait(&ct.tfull[b], tph, abort_flag))) break;
+            tc_fence_after();
+            const int blk = (t_begin + i) * kBM + row;
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * buf_cols);
+            for (int c0 = 0; c0 < qv * H; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+                for (int jj = 0; jj < 16 / H; ++jj) {
+                    const int j = c0 / H + jj;
+                    if (j < qv) {
+                        float s = 0.0f;
+#pragma unroll
+                        for (int h = 0; h < H; ++h)
+                            s = fmaf(ct.w[j * H + h], fmaxf(__uint_as_float(v[jj * H + h]), 0.0f), s);
+                        if (blk < ct.nb[j]) p.scores[(size_t)(q0 + j) * p.stride + blk] = s;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&ct.tempty[b]);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+    }
+    if (tid == 0 && ct.abort && p.flags) atomicOr(p.flags, QSA_FLAG_WAIT_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void *ptr;
+    uint64_t rows;
+    uint32_t box_rows;
+    int f32;
+    int dev;
+    bool operator==(const MapKey &o) const {
+        return ptr == o.ptr && rows == o.rows && box_rows == o.box_rows && f32 == o.f32 && dev == o.dev;
+    }
+};
+
+// Small cache of encoded tensor maps (a map is 128 bytes of host data).
+qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint64_t rows, uint32_t box_rows) {
+    static std::mutex mu;
+    static MapKey keys[32];
+    static CUtensorMap maps[32];
+    static int used = 0, next = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const MapKey key{ptr, rows, box_rows, f32 ? 1 : 0, dev};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (keys[i] == key) {
+                *out = maps[i];
+                return QSA_OK;
+            }
+    }
+    auto fn = encode_fn();
+    if (!fn) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)QSA_HEAD_DIM, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)QSA_HEAD_DIM * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    const CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        keys[next] = key;
+        maps[next] = m;
+        next = (next + 1) % 32;
+        if (used < 32) ++used;
+    }
+    *out = m;
+    return QSA_OK;
+}
+
+template <bool F32, int H>
+qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
+                        cudaStream_t s) {
+    constexpr int bytes = smem_bytes<F32>();
+    static_assert(bytes <= 227 * 1024, "scorer shared memory");
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(scorer_tc_kernel<F32, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    if (attr_err != cudaSuccess) return check_cuda(attr_err, "cudaFuncSetAttribute(scorer)");
+    scorer_tc_kernel<F32, H><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
+    return check_cuda(cudaGetLastError(), "scorer_tc_kernel launch");
+}
+
+template <bool F32>
+qsa_status launch_heads(int H, const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
+                        cudaStream_t s) {
+    switch (H) {
+    case 1: return launch_typed<F32, 1>(mk, mq, kp, grid, s);
+    case 2: return launch_typed<F32, 2>(mk, mq, kp, grid, s);
+    case 4: return launch_typed<F32, 4>(mk, mq, kp, grid, s);
+    case 8: return launch_typed<F32, 8>(mk, mq, kp, grid, s);
+    case 16: return launch_typed<F32, 16>(mk, mq, kp, grid, s);
+    default: return fail(QSA_ERR_INVALID_ARG, "n_heads %d", H);
+    }
+}
+
+}  // namespace
+
+qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
+    const bool f32 = a.dt == QSA_F32;
+    const int H = a.n_heads;
+    const int max_bn = f32 ? Cfg<true>::kMaxBN : Cfg<false>::kMaxBN;
+    const int qg = std::min(a.nq, std::max(1, max_bn / H));
+    const int bn = (qg * H + 15) / 16 * 16;
+    const int groups = (a.nq + qg - 1) / qg;
+    const int tiles = (a.bound + kBM - 1) / kBM;
+    if (tiles == 0) return QSA_OK;   // no block can be valid
+    const int sms = num_sms();
+    int cpg = std::max(1, std::min(tiles, sms / groups));
+    const int tpc = (tiles + cpg - 1) / cpg;
+    cpg = (tiles + tpc - 1) / tpc;
+    int tmem_cols = 32;
+    while (tmem_cols < 2 * bn) tmem_cols *= 2;
+
+    CUtensorMap mk, mq;
+    qsa_status st = get_map(&mk, a.kblk, f32, (uint64_t)a.max_blocks, kBM);
+    if (st != QSA_OK) return st;
+    st = get_map(&mq, a.q, f32, (uint64_t)a.nq * H, (uint32_t)bn);
+    if (st != QSA_OK) return st;
+
+    KParams kp{};
+    kp.w = a.w;
+    kp.n_blocks = a.n_blocks;
+    kp.scores = a.scores;
+    kp.stride = a.stride;
+    kp.flags = a.flags;
+    kp.nq = a.nq;
+    kp.bound = a.bound;
+    kp.qg = qg;
+    kp.bn = bn;
+    kp.tiles_per_cta = tpc;
+    kp.tmem_cols = tmem_cols;
+    const dim3 grid(cpg, groups);
+    return f32 ? launch_heads<true>(H, mk, mq, kp, grid, s) : launch_heads<false>(H, mk, mq, kp, grid, s);
+}
+
+}  // namespace qsa

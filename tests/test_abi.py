@@ -1,0 +1,110 @@
+"""The C-ABI library (CPU side): it loads, exports every symbol include/qsa.h
+declares, sizes workspaces, picks paths, and rejects bad arguments on the host
+before any launch.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_kv_gb300 import _build, qsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return qsa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(qsa.EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert lib.qsa_version() == 1
+
+
+def test_workspace_sizes(lib):
+    a = lib.qsa_workspace_bytes(256, 8192, 32, 0)
+    assert a > 256 and a % 256 == 0
+    assert lib.qsa_workspace_bytes(3, 4096, 32, 0) < a
+    for bad in ((0, 8192, 32), (1, 0, 32), (1, 8192, 0), (1, 8192, 1025), (1, (1 << 24) + 1, 8)):
+        assert lib.qsa_workspace_bytes(*bad, 0) == 0
+
+
+def test_auto_path_rules(lib):
+    # decode window (no active count, few queries): split
+    assert lib.qsa_auto_path(3, 4096, -1, 32) == qsa.PATH_SPLIT
+    assert lib.qsa_auto_path(16, 4096, -1, 32) == qsa.PATH_SPLIT
+    # prompt calls: sampled filter past the threshold, register below it
+    assert lib.qsa_auto_path(256, 8192, 8125, 32) == qsa.PATH_SAMPLE
+    assert lib.qsa_auto_path(256, 2048, 2048, 32) == qsa.PATH_SAMPLE
+    assert lib.qsa_auto_path(256, 8192, 1000, 32) == qsa.PATH_REGISTER
+    # beyond the on-chip reach: radix
+    assert lib.qsa_auto_path(256, 100000, 100000, 32) == qsa.PATH_RADIX
+    assert lib.qsa_auto_path(64, 100000, -1, 32) == qsa.PATH_RADIX
+
+
+FAKE = 0x10000   # never dereferenced: each call below fails validation first
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(q=None), qsa.ERR_INVALID_ARG),
+    (dict(head_dim=64), qsa.ERR_INVALID_ARG),
+    (dict(n_heads=3), qsa.ERR_INVALID_ARG),
+    (dict(n_heads=32), qsa.ERR_INVALID_ARG),
+    (dict(nq=0), qsa.ERR_INVALID_ARG),
+    (dict(max_blocks=0), qsa.ERR_INVALID_ARG),
+    (dict(stride=100), qsa.ERR_INVALID_ARG),
+    (dict(dt=7), qsa.ERR_INVALID_ARG),
+    (dict(q=FAKE + 4), qsa.ERR_INVALID_ARG),
+    (dict(active=-2), qsa.ERR_INVALID_ARG),
+    (dict(k=0), qsa.ERR_INVALID_ARG),
+    (dict(k=1025), qsa.ERR_INVALID_ARG),
+    (dict(ws=None), qsa.ERR_WORKSPACE),
+    (dict(ws_bytes=1024), qsa.ERR_WORKSPACE),
+    (dict(ws=FAKE + 64), qsa.ERR_WORKSPACE),
+])
+def test_select_rejects_bad_arguments_before_launch(lib, case, status):
+    a = dict(q=FAKE, w=FAKE, kblk=FAKE, dt=qsa.BF16, n_blocks=FAKE, nq=4, n_heads=16, head_dim=128,
+             max_blocks=1024, active=-1, k=32, ids=FAKE, scores=FAKE, stride=1024, fused=0, ws=FAKE,
+             ws_bytes=1 << 30, path=qsa.PATH_AUTO)
+    a.update(case)
+    st = lib.qsa_select(a["q"], a["w"], a["kblk"], a["dt"], a["n_blocks"], a["nq"], a["n_heads"],
+                        a["head_dim"], a["max_blocks"], a["active"], a["k"], a["ids"], a["scores"],
+                        a["stride"], a["fused"], a["ws"], a["ws_bytes"], a["path"], None)
+    assert st == status
+    assert lib.qsa_last_error().decode()
+
+
+def test_topk_rejects_bad_arguments_before_launch(lib):
+    st = lib.qsa_block_topk(FAKE, 100, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 0, None)
+    assert st == qsa.ERR_INVALID_ARG   # stride < max_blocks
+    st = lib.qsa_block_topk(FAKE, 1024, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 16, 0, None)
+    assert st == qsa.ERR_WORKSPACE
+    st = lib.qsa_block_topk(None, 1024, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 0, None)
+    assert st == qsa.ERR_INVALID_ARG
+    st = lib.qsa_block_topk(FAKE, 1024, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 9, None)
+    assert st == qsa.ERR_INVALID_ARG   # bad path enum
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(qsa, "_lib", None)
+    monkeypatch.setattr(qsa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        qsa.load()

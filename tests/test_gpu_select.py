@@ -1,0 +1,133 @@
+"""GPU parity of the scorer and of the whole select path on the five workloads.
+
+Rule (b) on the scores, rule (a) on the top-k of the GPU's own scores, rule (c)
+end to end against the FP64 oracle (see tests/parity.py).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_kv_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from sparse_attention_kv_gb300 import qsa  # noqa: E402
+
+
+def gpu_scores(case, active=None):
+    q, w, kb, nb = parity.to_device(case)
+    act = case.active_blocks if active is None else active
+    sc = torch.full((case.nq, case.max_blocks), float("nan"), dtype=torch.float32, device="cuda")
+    ws = qsa.alloc_workspace(case.nq, case.max_blocks, case.k)
+    qsa.block_scores(q, w, kb, nb, sc, active_blocks=act, ws=ws)
+    flags = qsa.read_flags(ws)
+    return sc.cpu().numpy(), flags
+
+
+def run_select(case, path=qsa.PATH_AUTO, fused=False):
+    q, w, kb, nb = parity.to_device(case)
+    sc = torch.full((case.nq, case.max_blocks), float("nan"), dtype=torch.float32, device="cuda")
+    ids = torch.full((case.nq, case.k), -7, dtype=torch.int32, device="cuda")
+    ws = qsa.alloc_workspace(case.nq, case.max_blocks, case.k, fused=fused)
+    qsa.select(q, w, kb, nb, case.k, ids, ws, scores=sc, fused=fused,
+               active_blocks=case.active_blocks, path=path)
+    flags = qsa.read_flags(ws)
+    return ids.cpu().numpy(), sc.cpu().numpy(), flags
+
+
+def full_check(case, path=qsa.PATH_AUTO):
+    ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
+    ref_ids = oracle.select(ref, case.n_blocks, case.k)
+    ids, sc, flags = run_select(case, path)
+    assert flags == 0, f"device flags {flags:#x}"
+    # scores are written exactly for b < n and left alone past it
+    for qi, n in enumerate(case.n_blocks):
+        assert np.isfinite(sc[qi, :n]).all()
+        assert np.isnan(sc[qi, n:]).all()
+    err = parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
+    parity.check_rule_a(ids, oracle.select_f32(sc, case.n_blocks, case.k))
+    r = parity.check_rule_c(ids, ref, ref_ids, case.n_blocks, case.k, case.dtype, tight_tol=4 * max(err, 1e-9))
+    print(f"{case.name}: max score err {err:.2e}; rule (c) {r['exact']}/{r['queries']} exact, "
+          f"{r['excused']} excused, near-ties {r['near_tie']} (tight {r['near_tie_tight']})")
+    return ids, sc, r
+
+
+def test_tiny_fp32():
+    full_check(inputs.tiny_case())
+
+
+@pytest.mark.parametrize("i", range(len(inputs.DECODE_TOKENS)))
+def test_decode_window(i):
+    full_check(inputs.decode_case(i))
+
+
+def test_prompt():
+    full_check(inputs.prompt_case())
+
+
+@pytest.mark.parametrize("i", range(len(inputs.DEEP_TOKENS)))
+def test_deep_prompt(i):
+    full_check(inputs.deep_case(i))
+
+
+@pytest.mark.parametrize("kind", ["equal_kblk", "w_zero", "ragged"])
+def test_stress_end_to_end(kind):
+    case = inputs.stress_case(kind)
+    ids, sc, r = full_check(case)
+    if kind in ("equal_kblk", "w_zero"):
+        # every score ties: the lowest block ids, exactly, no excusal
+        assert r["exact"] == r["queries"]
+        want = np.minimum(case.n_blocks[:, None], case.k)
+        np.testing.assert_array_equal(ids, np.tile(np.arange(case.k, dtype=np.int32), (case.nq, 1)))
+
+
+@pytest.mark.parametrize("path", [qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_SPLIT])
+def test_every_path_end_to_end_on_decode_and_prompt(path):
+    for case in (inputs.decode_case(1), inputs.prompt_case()):
+        try:
+            full_check(case, path)
+        except qsa.QSAError as e:
+            if e.status != qsa.ERR_UNSUPPORTED:
+                raise
+
+
+@pytest.mark.parametrize("H", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+def test_scorer_heads_and_dtypes(H, dtype):
+    """Every head count, both input types, a group split across CTAs and a ragged tail."""
+    nq = 37
+    toks = inputs.ragged_tokens(7000 + H, nq, 300)
+    case = inputs.make_case(7000 + H + 10 * dtype, nq, H, 300, dtype, toks, 8, active_blocks=300)
+    sc, flags = gpu_scores(case)
+    assert flags == 0
+    ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
+    parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
+    for qi, n in enumerate(case.n_blocks):
+        assert np.isnan(sc[qi, n:]).all()
+
+
+def test_scorer_active_count_never_changes_scores():
+    case = inputs.decode_case(5)
+    a, _ = gpu_scores(case, active=-1)
+    b, _ = gpu_scores(case, active=4032)
+    np.testing.assert_array_equal(a[:, :4032], b[:, :4032])
+
+
+def test_scorer_clamps_n_blocks_to_active_bound():
+    case = inputs.make_case(7100, 4, 16, 1024, inputs.BF16, [64 * 500, 64 * 1024, 64 * 10, 64], 32)
+    sc, flags = gpu_scores(case, active=600)
+    assert flags & qsa.FLAG_NBLOCKS_CLAMPED
+    assert np.isfinite(sc[1, :600]).all() and np.isnan(sc[1, 600:]).all()
+
+
+def test_select_is_deterministic():
+    case = inputs.deep_case(0)
+    a = run_select(case)
+    b = run_select(case)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
