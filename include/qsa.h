@@ -81,6 +81,8 @@ typedef void *qsa_stream; /* a cudaStream_t */
 #define QSA_FLAG_NBLOCKS_CLAMPED 0x1u /* some n_blocks[q] was < 0 or > its bound; clamped */
 #define QSA_FLAG_WAIT_TIMEOUT 0x2u    /* a kernel gave up a bounded wait; its outputs are invalid */
 #define QSA_FLAG_INTERNAL 0x4u        /* an internal consistency check failed */
+#define QSA_FLAG_SAMPLE_FALLBACK 0x8u /* not an error: some query of the sampled filter had too few
+                                         or too many candidates and was selected from its whole row */
 
 /*
  * Workspace size in bytes for calls with these sizes (any path, fused or not).

@@ -33,7 +33,7 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 // Shared scratch of the block-wide helpers.
-struct BlockScratch {
+struct __align__(16) BlockScratch {
     int warp_sums[32];
     uint32_t hist[256];
     uint32_t red[64];
@@ -67,99 +67,6 @@ struct Threshold {
     int above;
     int budget;
 };
-
-// Radix select of the k-th largest of the valid keys held by the block.
-// Each thread holds KPT keys; bit i of `valid` marks keys[i] valid.  Requires
-// 1 <= k <= number of valid keys.  The bits that all valid keys share (the common
-// prefix of the smallest and largest key) are skipped; the remaining bits are
-// taken 8 at a time, most significant first: a 256-bin histogram of the digit
-// among the keys that match the prefix so far (warp-aggregated shared atomics),
-// then a warp scan of the bins from the top finds the bin holding the k-th key.
-template <int NT, int KPT>
-__device__ Threshold radix_threshold(const uint32_t (&keys)[KPT], uint32_t valid, int k,
-                                     BlockScratch &sm) {
-    constexpr int NW = NT / 32;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    // block min / max of the valid keys
-    uint32_t mn = 0xffffffffu, mx = 0u;
-#pragma unroll
-    for (int i = 0; i < KPT; ++i)
-        if (valid >> i & 1u) {
-            mn = min(mn, keys[i]);
-            mx = max(mx, keys[i]);
-        }
-    mn = __reduce_min_sync(kFull, mn);
-    mx = __reduce_max_sync(kFull, mx);
-    if (lane == 0) {
-        sm.red[wid] = mn;
-        sm.red[32 + wid] = mx;
-    }
-    __syncthreads();
-    if (wid == 0) {
-        uint32_t a = lane < NW ? sm.red[lane] : 0xffffffffu;
-        uint32_t b = lane < NW ? sm.red[32 + lane] : 0u;
-        a = __reduce_min_sync(kFull, a);
-        b = __reduce_max_sync(kFull, b);
-        if (lane == 0) {
-            sm.misc[2] = (int)a;
-            sm.misc[3] = (int)b;
-        }
-    }
-    __syncthreads();
-    mn = (uint32_t)sm.misc[2];
-    mx = (uint32_t)sm.misc[3];
-    int hi = 32 - __clz((int)(mn ^ mx));   // bits [0, hi) vary; 0 when all keys are equal
-    uint32_t prefix = hi == 32 ? 0u : (mx & ~((1u << hi) - 1u));
-    int remaining = k;
-    while (hi > 0) {
-        const int lo = hi > 8 ? hi - 8 : 0;
-        const int nbins = 1 << (hi - lo);
-        for (int i = threadIdx.x; i < nbins; i += NT) sm.hist[i] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < KPT; ++i) {
-            const bool match = (valid >> i & 1u) && (hi == 32 || (keys[i] >> hi) == (prefix >> hi));
-            const uint32_t d = match ? (keys[i] >> lo) & (uint32_t)(nbins - 1) : 0xffffffffu;
-            const unsigned peers = __match_any_sync(kFull, d);
-            if (match && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[d], (uint32_t)__popc(peers));
-        }
-        __syncthreads();
-        if (wid == 0) {
-            // lane l owns bins nbins-1-8l-j, j = 0..7 (descending)
-            uint32_t c[8];
-            int sum = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int b = nbins - 1 - 8 * lane - j;
-                c[j] = b >= 0 ? sm.hist[b] : 0u;
-                sum += (int)c[j];
-            }
-            const int incl = warp_incl_scan(sum);
-            int run = incl - sum;
-            if (run < remaining && remaining <= incl) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (run + (int)c[j] >= remaining) {
-                        sm.misc[0] = nbins - 1 - 8 * lane - j;
-                        sm.misc[1] = run;
-                        break;
-                    }
-                    run += (int)c[j];
-                }
-            }
-        }
-        __syncthreads();
-        remaining -= sm.misc[1];
-        prefix |= (uint32_t)sm.misc[0] << lo;
-        hi = lo;
-        __syncthreads();
-    }
-    Threshold t;
-    t.T = prefix;
-    t.above = k - remaining;
-    t.budget = remaining;
-    return t;
-}
 
 // Ordered emit.  The block's keys are laid out in R rounds of E consecutive
 // elements per thread: element (r, e) of thread t comes at position
@@ -201,6 +108,238 @@ __device__ void ordered_emit(const uint32_t (&keys)[R * E], const int32_t (&ids)
         gt_base += total >> 16;
         eq_base += total & 0xffff;
     }
+}
+
+
+// ---------------------------------------------------------------------------
+// Selection over candidates held in shared memory (unordered lists).
+
+// Append the calling threads' items to a shared list with one atomic per warp.
+// Returns the list slot of this thread's first item.  All 32 lanes call.
+__device__ __forceinline__ int warp_append(int count, int *counter) {
+    const int lane = threadIdx.x & 31;
+    const int incl = warp_incl_scan(count);
+    int base = 0;
+    if (lane == 31 && incl > 0) base = atomicAdd(counter, incl);
+    base = __shfl_sync(kFull, base, 31);
+    return base + incl - count;
+}
+
+template <int NT>
+struct __align__(16) CandSmem {
+    static constexpr int NW = NT / 32;
+    uint32_t hist[256];   // one digit histogram; zero between passes
+    uint32_t wmin[NW], wmax[NW];
+    int misc[8];
+    int cnt[4];           // list counters
+};
+
+template <int NT>
+__device__ __forceinline__ void cand_smem_init(CandSmem<NT> &sm) {
+    for (int i = threadIdx.x; i < 256; i += NT) sm.hist[i] = 0u;
+    if (threadIdx.x < 4) sm.cnt[threadIdx.x] = 0;
+}
+
+// Block min and max of per-thread (mn, mx), returned to every thread (one barrier).
+template <int NT>
+__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, CandSmem<NT> &sm) {
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    const int wid = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sm.wmin[wid] = mn;
+        sm.wmax[wid] = mx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < CandSmem<NT>::NW; ++w) {
+        mn = min(mn, sm.wmin[w]);
+        mx = max(mx, sm.wmax[w]);
+    }
+}
+
+// k-th largest of the keys key_at(i), i < m, for which key_at returns true;
+// every such key lies in [mn, mx].  The bits mn and mx share are skipped, the
+// rest are taken 8 at a time from the top: a shared histogram of the digit over
+// the keys that match the prefix so far, then warp 0 scans the bins from the
+// highest down (clearing them) to find the bin of the k-th key.  Two barriers a
+// digit; the histogram must be zero on entry and is left zero.
+template <int NT, typename KeyAt>
+__device__ Threshold smem_threshold(KeyAt &&key_at, int m, int k, uint32_t mn, uint32_t mx,
+                                    CandSmem<NT> &sm) {
+    const int lane = threadIdx.x & 31;
+    int hi = 32 - __clz((int)(mn ^ mx));
+    uint32_t prefix = hi == 32 ? 0u : (mx & ~((1u << hi) - 1u));
+    int remaining = k;
+    while (hi > 0) {
+        const int lo = hi > 8 ? hi - 8 : 0;
+        const int nbins = 1 << (hi - lo);
+        for (int i = threadIdx.x; i < m; i += NT) {
+            uint32_t key;
+            if (key_at(i, key) && (hi == 32 || (key >> hi) == (prefix >> hi)))
+                atomicAdd(&sm.hist[(key >> lo) & (uint32_t)(nbins - 1)], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t c[8];
+            int sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int b = nbins - 1 - 8 * lane - j;
+                c[j] = 0u;
+                if (b >= 0) {
+                    c[j] = sm.hist[b];
+                    sm.hist[b] = 0u;
+                }
+                sum += (int)c[j];
+            }
+            const int incl = warp_incl_scan(sum);
+            int run = incl - sum;
+            if (run < remaining && remaining <= incl) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (run + (int)c[j] >= remaining) {
+                        sm.misc[0] = nbins - 1 - 8 * lane - j;
+                        sm.misc[1] = run;
+                        break;
+                    }
+                    run += (int)c[j];
+                }
+            }
+        }
+        __syncthreads();
+        remaining -= sm.misc[1];
+        prefix |= (uint32_t)sm.misc[0] << lo;
+        hi = lo;
+    }
+    Threshold t;
+    t.T = prefix;
+    t.above = k - remaining;
+    t.budget = remaining;
+    return t;
+}
+
+// The k selected candidates i < m: every key > T, and of the keys == T the
+// `budget` lowest ids (a second threshold over ~id among the ties when there
+// are more ties than budget).  key_at(i) gives candidate i's key, id_at(i) its
+// block id.  Appends ids (and keys, when sel_key is not null) to sel_id through
+// sm.cnt[0]; uses sm.cnt[1].  Both counters must be zero on entry.  Ends with a
+// barrier, after which sm.cnt[0] == k.
+template <int NT, typename KeyAt, typename IdAt>
+__device__ void collect_smem(KeyAt &&key_at, IdAt &&id_at, int m, const Threshold &th, uint32_t *sel_key,
+                             int32_t *sel_id, CandSmem<NT> &sm) {
+    int neq = 0;
+    for (int base = 0; base < m; base += NT) {
+        const int i = base + (int)threadIdx.x;
+        const uint32_t key = i < m ? key_at(i) : 0u;
+        const bool gt = i < m && key > th.T;
+        neq += (i < m && key == th.T);
+        const int pos = warp_append(gt ? 1 : 0, &sm.cnt[0]);
+        if (gt) {
+            if (sel_key) sel_key[pos] = key;
+            sel_id[pos] = id_at(i);
+        }
+    }
+    const int wt = (int)__reduce_add_sync(kFull, (unsigned)neq);
+    if ((threadIdx.x & 31) == 0 && wt) atomicAdd(&sm.cnt[1], wt);
+    __syncthreads();
+    const int ntie = sm.cnt[1];
+    uint32_t T2 = 0u;   // ties with ~id >= T2 are taken; all of them when T2 == 0
+    if (ntie > th.budget) {
+        const Threshold t2 = smem_threshold<NT>(
+            [&](int i, uint32_t &key) {
+                if (key_at(i) != th.T) return false;
+                key = ~(uint32_t)id_at(i);
+                return true;
+            },
+            m, th.budget, 0u, 0xffffffffu, sm);
+        T2 = t2.T;
+    }
+    for (int base = 0; base < m; base += NT) {
+        const int i = base + (int)threadIdx.x;
+        const bool take = i < m && key_at(i) == th.T && ~(uint32_t)id_at(i) >= T2;
+        const int pos = warp_append(take ? 1 : 0, &sm.cnt[0]);
+        if (take) {
+            if (sel_key) sel_key[pos] = th.T;
+            sel_id[pos] = id_at(i);
+        }
+    }
+    __syncthreads();
+}
+
+// Sort n (<= 1024) ids held in shared memory ascending and write them to out,
+// padded with -1 up to k.  n <= 32: warp 0 sorts them in registers (bitonic);
+// else a bitonic sort in shared memory over the next power of two (`buf` must
+// hold that many ints).  Every thread of the block calls it.
+template <int NT>
+__device__ void sort_emit(int32_t *buf, int n, int k, int32_t *out) {
+    const int lane = threadIdx.x & 31;
+    if (n <= 32) {
+        if (threadIdx.x < 32) {
+            int v = lane < n ? buf[lane] : 0x7fffffff;
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const int o = __shfl_xor_sync(kFull, v, stride);
+                    const bool up = (lane & size) == 0;
+                    const bool lower = (lane & stride) == 0;
+                    v = (lower == up) ? min(v, o) : max(v, o);
+                }
+            }
+            if (lane < n) out[lane] = v;
+        }
+    } else {
+        int P = 64;
+        while (P < n) P <<= 1;
+        for (int i = n + threadIdx.x; i < P; i += NT) buf[i] = 0x7fffffff;
+        __syncthreads();
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = threadIdx.x; i < P / 2; i += NT) {
+                    const int lo = 2 * i - (i & (stride - 1));
+                    const int hi = lo + stride;
+                    const bool up = (lo & size) == 0;
+                    const int a = buf[lo], b = buf[hi];
+                    if ((a > b) == up) {
+                        buf[lo] = b;
+                        buf[hi] = a;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int i = threadIdx.x; i < n; i += NT) out[i] = buf[i];
+    }
+    for (int i = n + threadIdx.x; i < k; i += NT) out[i] = -1;
+}
+
+// One warp: the r-th largest (1 <= r <= n) of n <= 256 keys, held 8 per lane
+// (lane l has v[l + 32e]; absent entries are 0, below every score key).  Each
+// lane sorts its 8 keys descending, then r rounds take the warp maximum of the
+// lanes' heads and advance the first lane holding it.
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t (&x)[8], int r) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j = 0; j < 7 - i; ++j) {
+            const uint32_t a = x[j], b = x[j + 1];
+            x[j] = max(a, b);
+            x[j + 1] = min(a, b);
+        }
+    }
+    uint32_t res = 0u;
+    for (int it = 0; it < r; ++it) {
+        res = __reduce_max_sync(kFull, x[0]);
+        const unsigned win = __ballot_sync(kFull, x[0] == res);
+        if (lane == __ffs(win) - 1) {
+#pragma unroll
+            for (int j = 0; j < 7; ++j) x[j] = x[j + 1];
+            x[7] = 0u;
+        }
+    }
+    return res;
 }
 
 }  // namespace qsa

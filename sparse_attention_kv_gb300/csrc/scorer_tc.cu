@@ -36,7 +36,8 @@ namespace qsa {
 namespace {
 
 constexpr int kBM = 128;       // KV blocks per tile (MMA M = TMEM lanes)
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 576;  // 18 warps: TMA, MMA, 16 epilogue
+constexpr int kEpi = 512;      // epilogue threads
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
 
 template <bool F32>
@@ -75,7 +76,7 @@ struct Ctrl {
     int abort;
     int maxn;
     int pad;
-    float w[256];
+    __align__(16) float w[256];
     int nb[256];
 };
 
@@ -88,7 +89,7 @@ struct KParams {
     float *scores;
     int64_t stride;
     uint32_t *flags;
-    int nq, bound, qg, bn, tiles_per_cta, tmem_cols;
+    int nq, bound, qg, bn, tiles_per_cta, tiles_total, tmem_cols;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -122,13 +123,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// One try_wait that may suspend the thread (up to ~65 us, or until the phase
+// completes), so waiting warps take no issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(65536u)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase of parity `parity` to complete.  Gives up when another
 // thread has aborted or after kWaitNs (then raises the abort itself).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = now_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
         if (now_ns() - t0 > kWaitNs) {
             *abort_flag = 1;
@@ -181,15 +195,62 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Ties loaded registers to a point after tcgen05.wait::ld, so that no use of
+// them is scheduled before the wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&v)[16]) {
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]));
+}
+
+// sum_h w[h] * relu(acc[h]) for one query, in fp32: ReLU per head, then the
+// products added in two interleaved partial sums (packed two-wide FMA) that
+// are combined at the end.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+template <int H>
+__device__ __forceinline__ float head_sum(const float *w, const uint32_t *acc) {
+    if constexpr (H >= 4) {
+        uint64_t s = 0;   // (0.0f, 0.0f)
+#pragma unroll
+        for (int h = 0; h < H; h += 4) {
+            const float4 wv = *reinterpret_cast<const float4 *>(w + h);
+            const float r0 = fmaxf(__uint_as_float(acc[h + 0]), 0.0f);
+            const float r1 = fmaxf(__uint_as_float(acc[h + 1]), 0.0f);
+            const float r2 = fmaxf(__uint_as_float(acc[h + 2]), 0.0f);
+            const float r3 = fmaxf(__uint_as_float(acc[h + 3]), 0.0f);
+            s = fma2(pack2(wv.x, wv.y), pack2(r0, r1), s);
+            s = fma2(pack2(wv.z, wv.w), pack2(r2, r3), s);
+        }
+        float a, b;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(s));
+        return a + b;
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < H; ++h) s = fmaf(w[h], fmaxf(__uint_as_float(acc[h]), 0.0f), s);
+        return s;
+    }
+}
+
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
@@ -250,6 +311,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qv = min(p.qg, p.nq - q0);  // queries of this group
     const int bn = p.bn;
 
+    const int t_begin = blockIdx.x * p.tiles_per_cta;
+    const int t_cap = min(p.tiles_per_cta, p.tiles_total - t_begin);  // tiles under the bound
+
+    if (tid == 32) {
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&ct.full[s], 1);
+            mbar_init(&ct.empty[s], 1);
+            mbar_init(&ct.split[s], kEpi);
+        }
+        mbar_init(&ct.bfull, 1);
+        mbar_init(&ct.bsplit, kEpi);
+        mbar_init(&ct.done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ct.tfull[b], 1);
+            mbar_init(&ct.tempty[b], kEpi);
+        }
+        ct.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    }
+    __syncthreads();
+    // The query tile and the first stages are requested before the group's block
+    // counts are known, so their latency overlaps the reads of w and n_blocks.
+    int issued = 0;
+    if (tid == 0) {
+        mbar_expect_tx(&ct.bfull, (uint32_t)(C::kAtoms * bn * 128));
+        for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_2d(sB + a * bn * 128, &tm_q, &ct.bfull, a * C::kEPA, q0 * H);
+        const int pre = min(C::kStages, t_cap);
+        for (int i = 0; i < pre; ++i) {
+            mbar_expect_tx(&ct.full[i], (uint32_t)(C::kAtoms * kAtomA));
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_2d(sA + i * L::kAStage + a * kAtomA, &tm_k, &ct.full[i], a * C::kEPA, (t_begin + i) * kBM);
+        }
+        issued = pre;
+    }
     for (int i = tid; i < qv * H; i += kThreads) ct.w[i] = p.w[(size_t)q0 * H + i];
     if (warp == 0) {
         int mx = 0;
@@ -265,27 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) ct.maxn = mx;
     }
-    if (tid == 32) {
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&ct.full[s], 1);
-            mbar_init(&ct.empty[s], 1);
-            mbar_init(&ct.split[s], 128);
-        }
-        mbar_init(&ct.bfull, 1);
-        mbar_init(&ct.bsplit, 128);
-        mbar_init(&ct.done, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&ct.tfull[b], 1);
-            mbar_init(&ct.tempty[b], 128);
-        }
-        ct.abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
     __syncthreads();
     const int ntiles_g = (ct.maxn + kBM - 1) / kBM;
-    const int t_begin = blockIdx.x * p.tiles_per_cta;
     const int ntiles = min(t_begin + p.tiles_per_cta, ntiles_g) - t_begin;
-    if (ntiles <= 0) return;
+    if (ntiles <= 0) {
+        if (tid == 0) {   // nothing to compute: let the early loads land before exiting
+            for (int j = 0; j < issued; ++j) mbar_drain(&ct.full[j], 0);
+            mbar_drain(&ct.bfull, 0);
+        }
+        return;
+    }
 
     if (warp == 1) {
         tmem_alloc(&ct.tmem_base, (uint32_t)p.tmem_cols);
@@ -299,14 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- producer
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-            mbar_expect_tx(&ct.bfull, (uint32_t)(C::kAtoms * bn * 128));
-            for (int a = 0; a < C::kAtoms; ++a)
-                tma_load_2d(sB + a * bn * 128, &tm_q, &ct.bfull, a * C::kEPA, q0 * H);
-            int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
+            // ---------------- producer (tiles after the early ones)
+            for (int i = issued; i < ntiles; ++i) {
                 const int s = i % C::kStages;
                 const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
                 if (!mbar_wait(&ct.empty[s], ph ^ 1u, abort_flag)) break;
@@ -362,14 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(&ct.done, 0);
         }
     } else {
-        // ---------------- epilogue: warps 2..5, one accumulator row per thread
-        const int et = tid - 64;                 // 0..127
+        // ---------------- epilogue: warps 2..17, one accumulator row per thread.
+        // The four warps of a TMEM lane quarter (warp % 4) split the tile's
+        // 16-column chunks (16/H queries each) into four parts.
+        const int et = tid - 64;                 // 0..511
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const int part = (warp - 2) >> 2;        // 0..3
         const int row = quarter * 32 + lane;
+        const int nchunk = (qv * H + 15) / 16;   // <= 16
+        const int c_begin = part * nchunk / 4;
+        const int c_end = (part + 1) * nchunk / 4;
         bool ok = true;
         if constexpr (F32) {
             ok = __all_sync(0xffffffffu, mbar_wait(&ct.bfull, 0, abort_flag));
-            if (ok) split_tf32(sB, sBlo, C::kAtoms * bn * 128, et, 128);
+            if (ok) split_tf32(sB, sBlo, C::kAtoms * bn * 128, et, kEpi);
             fence_proxy_async();
             mbar_arrive(&ct.bsplit);
         }
@@ -378,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = i % C::kStages;
                 const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&ct.full[s], ph, abort_flag))) break;
-                split_tf32(sA + s * L::kAStage, sAlo + s * L::kAStage, L::kAStage, et, 128);
+                split_tf32(sA + s * L::kAStage, sAlo + s * L::kAStage, L::kAStage, et, kEpi);
                 fence_proxy_async();
                 mbar_arrive(&ct.split[s]);
             }
@@ -389,18 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int blk = (t_begin + i) * kBM + row;
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * buf_cols);
-            for (int c0 = 0; c0 < qv * H; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(taddr + (uint32_t)c0, v);
+            // every column chunk of this thread's part in flight at once, one wait
+            const int nc = c_end - c_begin;   // <= 4
+            uint32_t v[4][16];
 #pragma unroll
-                for (int jj = 0; jj < 16 / H; ++jj) {
-                    const int j = c0 / H + jj;
-                    if (j < qv) {
-                        float s = 0.0f;
+            for (int cc = 0; cc < 4; ++cc)
+                if (cc < nc) tmem_ld16_nowait(taddr + (uint32_t)((c_begin + cc) * 16), v[cc]);
+            tmem_wait_ld();
 #pragma unroll
-                        for (int h = 0; h < H; ++h)
-                            s = fmaf(ct.w[j * H + h], fmaxf(__uint_as_float(v[jj * H + h]), 0.0f), s);
-                        if (blk < ct.nb[j]) p.scores[(size_t)(q0 + j) * p.stride + blk] = s;
+            for (int cc = 0; cc < 4; ++cc)
+                if (cc < nc) reg_fence(v[cc]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (cc < nc) {
+#pragma unroll
+                    for (int jj = 0; jj < 16 / H; ++jj) {
+                        const int j = (c_begin + cc) * (16 / H) + jj;
+                        if (j < qv) {
+                            const float sc = head_sum<H>(&ct.w[j * H], &v[cc][jj * H]);
+                            if (blk < ct.nb[j]) p.scores[(size_t)(q0 + j) * p.stride + blk] = sc;
+                        }
                     }
                 }
             }
@@ -547,6 +644,7 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     kp.qg = qg;
     kp.bn = bn;
     kp.tiles_per_cta = tpc;
+    kp.tiles_total = tiles;
     kp.tmem_cols = tmem_cols;
     const dim3 grid(cpg, groups);
     return f32 ? launch_heads<true>(H, mk, mq, kp, grid, s) : launch_heads<false>(H, mk, mq, kp, grid, s);

@@ -2,17 +2,18 @@
 //
 // Four paths, all giving the ids of the rule in qsa_device.cuh:
 //  * register: one CTA per query holds its whole row in registers (<= 8,192
-//    blocks) and selects with no re-read -- the "register kernel" the pages name
-//    for contexts within its reach (Strata PR #3987, "Problem and result").
-//  * sample:   one CTA per query reads its row once; a lower bound LB taken as the
-//    KS-th largest key among every 32nd block (KS = 2k/32 + 16) keeps the keys
-//    >= LB as candidates on chip; with at least k and at most 4,096 candidates
-//    the threshold, "above" and the tie budget over the candidates equal the
-//    row's, else the query is flagged for the radix kernel ("#2093 sm_75: the
-//    prompt path's top-k with one full read of the scores", steps 1-4).
+//    blocks: 256 threads x 32) and selects with no re-read -- the "register
+//    kernel" the pages name for contexts within its reach (Strata PR #3987,
+//    "Problem and result").
+//  * sample:   the same kernel with the one-read candidate filter of "#2093 sm_75:
+//    the prompt path's top-k with one full read of the scores" (steps 1-4): a
+//    lower bound LB = the KS-th largest key among blocks 0, 32, 64, ...
+//    (KS = 2k/32 + 16); the blocks with score >= LB go to shared memory; with at
+//    least k and at most 4,096 of them the threshold, "above" and the tie budget
+//    over the candidates are the row's.  Otherwise the query falls back -- here
+//    to a select over the row it already holds on chip, with no second read.
 //  * radix:    one CTA per query, multi-pass radix select straight from global
-//    memory (four digit passes and the emit); any row length.  It is the
-//    fallback of the sampled filter (run for flagged queries only).
+//    memory (four digit passes and the emit); any row length.
 //  * split:    stage A, one CTA per (query, chunk), keeps the chunk's top-k
 //    candidates in the workspace; the last CTA of a query to finish (atomic
 //    ticket, nothing waits) runs stage B over the candidates.  A query's
@@ -79,143 +80,160 @@ __device__ __forceinline__ void row_ids(int base, int32_t (&ids)[R * 4]) {
     for (int i = 0; i < R * 4; ++i) ids[i] = base + (i / 4) * NT * 4 + (int)threadIdx.x * 4 + (i % 4);
 }
 
-// ---------------------------------------------------------------------------- register
+// ---------------------------------------------------------------------------- register / sample
 
-template <int NT, int R>
-__global__ void __launch_bounds__(NT) topk_register_kernel(TopkArgs a) {
-    __shared__ BlockScratch sm;
-    const int q = blockIdx.x;
-    const int k = a.k;
-    const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
-    int32_t *out = a.ids + (size_t)q * a.k;
-    if (n <= a.k) {
-        emit_all(n, a.k, out);
-        return;
-    }
-    if (n > NT * 4 * R) {   // cannot happen: the host sizes R from the bound
-        if (threadIdx.x == 0) atomicOr(a.flags, QSA_FLAG_INTERNAL);
-        emit_all(0, a.k, out);
-        return;
-    }
-    uint32_t keys[R * 4];
-    int32_t ids[R * 4];
-    const uint32_t valid = load_row_keys<NT, R>(a.scores + (size_t)q * a.stride, n, keys);
-    row_ids<NT, R>(0, ids);
-    const Threshold th = radix_threshold<NT, R * 4>(keys, valid, a.k, sm);
-    int gb = 0, eb = 0;
-    ordered_emit<NT, R, 4>(keys, ids, valid, th,
-                           [&](int slot, uint32_t, int32_t id) { if (slot < k) out[slot] = id; }, sm, gb, eb);
+constexpr int kNT = 256;   // threads of the register, sample and split kernels
+
+__device__ __forceinline__ float nan_pad() { return __int_as_float(0x7fffffff); }
+
+// Inverse of score_key (for keys of non-NaN scores).
+__device__ __forceinline__ float key_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
-// ---------------------------------------------------------------------------- sample
+// Row values striped over the block: round r, thread t, component e holds
+// position r*kNT*4 + t*4 + e.  Positions at or past n read as NaN, which no
+// comparison selects.  float4 streaming loads when the row is 16-byte aligned.
+template <int R>
+__device__ __forceinline__ void load_row_vals(const float *row, int n, float (&x)[R * 4]) {
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int p = r * kNT * 4 + (int)threadIdx.x * 4;
+        if (vec && p + 3 < n) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(row + p));
+            x[r * 4 + 0] = v.x;
+            x[r * 4 + 1] = v.y;
+            x[r * 4 + 2] = v.z;
+            x[r * 4 + 3] = v.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[r * 4 + e] = p + e < n ? __ldcs(row + p + e) : nan_pad();
+        }
+    }
+}
 
-template <int NT, int R>
-__global__ void __launch_bounds__(NT) topk_sample_kernel(TopkArgs a) {
-    constexpr int RC = kSampleCap / NT;          // candidate rounds per thread
-    constexpr int kMaxSamples = NT * 4 * R / 32;
-    __shared__ BlockScratch sm;
-    __shared__ uint32_t cand_key[kSampleCap];
-    __shared__ int32_t cand_id[kSampleCap];
-    __shared__ uint32_t samples[kMaxSamples];
+__device__ __forceinline__ int striped_id(int i) { return (i >> 2) * kNT * 4 + (int)threadIdx.x * 4 + (i & 3); }
+
+struct __align__(16) RowSmem {
+    CandSmem<kNT> cs;
+    // sample path: candidate scores in cand[0, 4096), their ids in cand[4096, 8192);
+    // whole-row select: every score of the row, in block order (ids implicit)
+    uint32_t cand[kRegisterCap];
+    int32_t sel[1024];
+};
+
+template <int R, bool SAMPLE>
+__global__ void __launch_bounds__(kNT, 2) topk_row_kernel(TopkArgs a) {
+    constexpr int KPT = R * 4;
+    static_assert(2 * kSampleCap == kRegisterCap, "candidate scores and ids share cand[]");
+    __shared__ RowSmem sm;
+    float *cval = reinterpret_cast<float *>(sm.cand);
+    int32_t *cid = reinterpret_cast<int32_t *>(sm.cand + kSampleCap);
     const int q = blockIdx.x;
     const int k = a.k;
     const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
     int32_t *out = a.ids + (size_t)q * k;
     if (n <= k) {
         emit_all(n, k, out);
-        if (threadIdx.x == 0) a.qflags[q] = 0u;
         return;
     }
-    if (n > NT * 4 * R) {
-        if (threadIdx.x == 0) a.qflags[q] = 1u;
+    if (n > kNT * KPT) {   // cannot happen: the host sizes R from the bound
+        if (threadIdx.x == 0) atomicOr(a.flags, QSA_FLAG_INTERNAL);
+        emit_all(0, k, out);
         return;
     }
-    uint32_t keys[R * 4];
-    int32_t ids[R * 4];
-    const uint32_t valid = load_row_keys<NT, R>(a.scores + (size_t)q * a.stride, n, keys);
-    row_ids<NT, R>(0, ids);
-
-    // 1. the bound: KS-th largest key among blocks 0, 32, 64, ...
+    const float *row = a.scores + (size_t)q * a.stride;
+    cand_smem_init(sm.cs);
     const int ns = (n + 31) / 32;
     const int KS = 2 * k / 32 + 16;
-    if ((threadIdx.x & 7) == 0) {
+    const bool sampled = SAMPLE && ns >= KS;   // fewer samples than KS: every block is a candidate
+    // 1. warp 0 reads the samples (blocks 0, 32, 64, ...) before the row, so the
+    //    bound is computed while the rest of the row is still arriving
+    uint32_t skey[8];
+    if (sampled && threadIdx.x < 32) {
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (valid >> (r * 4) & 1u) samples[(r * NT * 4 + (int)threadIdx.x * 4) / 32] = keys[r * 4];
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        uint32_t lb = 0u;   // fewer samples than KS: every key is a candidate
-        if (ns >= KS) {
-            constexpr int SPL = (kMaxSamples + 31) / 32;
-            uint32_t s[SPL];
-#pragma unroll
-            for (int j = 0; j < SPL; ++j) {
-                const int idx = j * 32 + (int)threadIdx.x;
-                s[j] = idx < ns ? samples[idx] : 0u;   // key 0 is below every finite score
-            }
-            for (int bit = 31; bit >= 0; --bit) {
-                const uint32_t c = lb | (1u << bit);
-                int cnt = 0;
-#pragma unroll
-                for (int j = 0; j < SPL; ++j) cnt += s[j] >= c;
-                cnt = (int)__reduce_add_sync(kFull, (unsigned)cnt);
-                if (cnt >= KS) lb = c;
-            }
+        for (int e = 0; e < 8; ++e) {
+            const int j = (int)threadIdx.x + 32 * e;
+            skey[e] = j < ns ? score_key(__ldg(row + 32 * j)) : 0u;
         }
-        if (threadIdx.x == 0) sm.misc[4] = (int)lb;
+    }
+    float x[KPT];
+    load_row_vals<R>(row, n, x);
+    if (sampled && threadIdx.x < 32) {
+        const uint32_t lbk = warp_kth_largest(skey, KS);
+        if (threadIdx.x == 0) sm.cs.misc[4] = (int)lbk;
     }
     __syncthreads();
-    const uint32_t lb = (uint32_t)sm.misc[4];
+    const float lb = sampled ? key_float((uint32_t)sm.cs.misc[4]) : -__int_as_float(0x7f800000);
 
-    // 2. one pass over the row: keys >= LB go to shared memory, in block order
-    int m = 0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
+    bool done = false;
+    if (SAMPLE || n <= kSampleCap) {
+        // 2. one pass over the row held on chip: blocks with score >= LB become
+        //    candidates (score, id) in shared memory, in any order
         int c = 0;
+        float tmax = -__int_as_float(0x7f800000);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c += (valid >> (r * 4 + e) & 1u) && keys[r * 4 + e] >= lb;
-        int total;
-        int pos = m + block_excl_scan<NT>(c, sm, total);
+        for (int i = 0; i < KPT; ++i) {
+            c += x[i] >= lb;
+            tmax = fmaxf(tmax, x[i]);
+        }
+        int pos = warp_append(c, &sm.cs.cnt[2]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = r * 4 + e;
-            if ((valid >> i & 1u) && keys[i] >= lb) {
+        for (int i = 0; i < KPT; ++i)
+            if (x[i] >= lb) {
                 if (pos < kSampleCap) {
-                    cand_key[pos] = keys[i];
-                    cand_id[pos] = ids[i];
+                    cval[pos] = x[i];
+                    cid[pos] = striped_id(i);
                 }
                 ++pos;
             }
+        uint32_t mn = score_key(lb), mx = score_key(tmax);
+        block_minmax<kNT>(mn, mx, sm.cs);
+        const int m = sm.cs.cnt[2];
+        if (m >= k && m <= kSampleCap) {
+            // 3. at least k candidates: the threshold, "above" and the tie budget
+            //    over the candidates are the row's
+            const Threshold th = smem_threshold<kNT>(
+                [&](int i, uint32_t &key) {
+                    key = score_key(cval[i]);
+                    return true;
+                },
+                m, k, mn, mx, sm.cs);
+            collect_smem<kNT>([&](int i) { return score_key(cval[i]); }, [&](int i) { return cid[i]; }, m, th,
+                              nullptr, sm.sel, sm.cs);
+            done = true;
+        } else if (SAMPLE && threadIdx.x == 0) {
+            atomicOr(a.flags, QSA_FLAG_SAMPLE_FALLBACK);
         }
-        m += total;
     }
-    // 3./4. enough candidates and not too many: select among them; else flag
-    if (m < k || m > kSampleCap) {
-        if (threadIdx.x == 0) a.qflags[q] = 1u;
-        return;
-    }
-    __syncthreads();
-    uint32_t ck[RC];
-    int32_t ci[RC];
-    uint32_t cvalid = 0;
+    if (!done) {
+        // 4. select over the whole row, still on chip: its scores go to shared
+        //    memory in block order
+        __syncthreads();   // candidate lists are dead
+        float *rowv = reinterpret_cast<float *>(sm.cand);
+        uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
-    for (int r = 0; r < RC; ++r) {
-        const int idx = r * NT + (int)threadIdx.x;
-        if (idx < m) {
-            ck[r] = cand_key[idx];
-            ci[r] = cand_id[idx];
-            cvalid |= 1u << r;
-        } else {
-            ck[r] = 0u;
-            ci[r] = -1;
+        for (int i = 0; i < KPT; ++i) {
+            if (x[i] == x[i]) {   // not a padding NaN
+                const uint32_t key = score_key(x[i]);
+                mn = min(mn, key);
+                mx = max(mx, key);
+                rowv[striped_id(i)] = x[i];
+            }
         }
+        if (threadIdx.x < 4) sm.cs.cnt[threadIdx.x] = 0;
+        block_minmax<kNT>(mn, mx, sm.cs);
+        const Threshold th = smem_threshold<kNT>(
+            [&](int i, uint32_t &key) {
+                key = score_key(rowv[i]);
+                return true;
+            },
+            n, k, mn, mx, sm.cs);
+        collect_smem<kNT>([&](int i) { return score_key(rowv[i]); }, [&](int i) { return i; }, n, th, nullptr,
+                          sm.sel, sm.cs);
     }
-    const Threshold th = radix_threshold<NT, RC>(ck, cvalid, k, sm);
-    int gb = 0, eb = 0;
-    ordered_emit<NT, RC, 1>(ck, ci, cvalid, th,
-                            [&](int slot, uint32_t, int32_t id) { if (slot < k) out[slot] = id; }, sm, gb, eb);
-    if (threadIdx.x == 0) a.qflags[q] = 0u;
+    sort_emit<kNT>(sm.sel, k, k, out);
 }
 
 // ---------------------------------------------------------------------------- radix
@@ -297,10 +315,17 @@ __global__ void __launch_bounds__(NT) topk_radix_kernel(TopkArgs a, int flagged_
 
 // ---------------------------------------------------------------------------- split
 
-template <int NT, int RB>
-__global__ void __launch_bounds__(NT) topk_split_kernel(TopkArgs a, int chunk_len) {
-    __shared__ BlockScratch sm;
-    __shared__ int s_last;
+struct __align__(16) SplitSmem {
+    CandSmem<kNT> cs;
+    uint32_t ck[kSplitSlots];
+    int32_t cid[kSplitSlots];
+    uint32_t skey[1024];
+    int32_t sid[1024];
+    int last;
+};
+
+__global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chunk_len) {
+    __shared__ SplitSmem sm;
     const int q = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
     const int k = a.k;
     const int n = clamp_blocks(a.n_blocks, q, a.bound, c == 0 ? a.flags : nullptr);
@@ -308,105 +333,116 @@ __global__ void __launch_bounds__(NT) topk_split_kernel(TopkArgs a, int chunk_le
     uint32_t *ck = a.ckeys + slot0;
     int32_t *ci = a.cids + slot0;
 
-    // stage A: this chunk's candidates, in block order
+    // stage A: this chunk's k candidates (key, id), any order
     if (n > k) {
         const int lo = c * chunk_len;
         const int len = max(0, min(chunk_len, n - lo));
         const float *row = a.scores + (size_t)q * a.stride + lo;
         if (len <= k) {
-            for (int i = threadIdx.x; i < len; i += NT) {
+            for (int i = threadIdx.x; i < len; i += kNT) {
                 ck[i] = score_key(__ldcs(row + i));
                 ci[i] = lo + i;
             }
         } else {
-            uint32_t keys[4];
-            int32_t ids[4];
-            const uint32_t valid = load_row_keys<NT, 1>(row, len, keys);
-            row_ids<NT, 1>(lo, ids);
-            const Threshold th = radix_threshold<NT, 4>(keys, valid, k, sm);
-            int gb = 0, eb = 0;
-            ordered_emit<NT, 1, 4>(keys, ids, valid, th,
-                                   [&](int slot, uint32_t key, int32_t id) {
-                                       if (slot < k) {
-                                           ck[slot] = key;
-                                           ci[slot] = id;
-                                       }
-                                   },
-                                   sm, gb, eb);
+            cand_smem_init(sm.cs);
+            uint32_t mn = 0xffffffffu, mx = 0u;
+            for (int i = threadIdx.x; i < len; i += kNT) {
+                const uint32_t key = score_key(__ldcs(row + i));
+                sm.ck[i] = key;
+                mn = min(mn, key);
+                mx = max(mx, key);
+            }
+            block_minmax<kNT>(mn, mx, sm.cs);
+            const Threshold th = smem_threshold<kNT>(
+                [&](int i, uint32_t &key) {
+                    key = sm.ck[i];
+                    return true;
+                },
+                len, k, mn, mx, sm.cs);
+            collect_smem<kNT>([&](int i) { return sm.ck[i]; }, [&](int i) { return lo + i; }, len, th, sm.skey,
+                              sm.sid, sm.cs);
+            for (int i = threadIdx.x; i < k; i += kNT) {
+                ck[i] = sm.skey[i];
+                ci[i] = sm.sid[i];
+            }
         }
         if (threadIdx.x == 0) a.counts[(size_t)q * a.maxch + c] = min(len, k);
     }
-    // last CTA of the query to arrive runs stage B; no CTA waits for another
+    // the last CTA of the query to arrive runs stage B; no CTA waits for another
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned t = atomicAdd(&a.tickets[q], 1u);
-        s_last = (t == (unsigned)nch - 1u);
+        sm.last = (t == (unsigned)nch - 1u);
     }
     __syncthreads();
-    if (!s_last) return;
+    if (!sm.last) return;
     __threadfence();
     int32_t *out = a.ids + (size_t)q * k;
     if (n <= k) {
         emit_all(n, k, out);
     } else {
-        // slots c*k + j of every chunk, chunk-major: block order
-        uint32_t keys[RB];
-        int32_t ids[RB];
-        uint32_t valid = 0;
+        cand_smem_init(sm.cs);
+        __syncthreads();
         const uint32_t *qk = a.ckeys + (size_t)q * a.maxch * k;
         const int32_t *qi = a.cids + (size_t)q * a.maxch * k;
         const int32_t *qc = a.counts + (size_t)q * a.maxch;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            const int s = r * NT + (int)threadIdx.x;
-            const int cc = s / k, j = s - cc * k;
-            keys[r] = 0u;
-            ids[r] = -1;
-            if (cc < nch && j < __ldcg(qc + cc)) {
-                keys[r] = __ldcg(qk + s);
-                ids[r] = __ldcg(qi + s);
-                valid |= 1u << r;
+        const int slots = nch * k;
+        uint32_t mn = 0xffffffffu, mx = 0u;
+        for (int base = 0; base < slots; base += kNT) {
+            const int s = base + (int)threadIdx.x;
+            const int cc = s / k;
+            const bool v = s < slots && (s - cc * k) < __ldcg(qc + cc);
+            const int pos = warp_append(v ? 1 : 0, &sm.cs.cnt[2]);
+            if (v) {
+                const uint32_t key = __ldcg(qk + s);
+                sm.ck[pos] = key;
+                sm.cid[pos] = __ldcg(qi + s);
+                mn = min(mn, key);
+                mx = max(mx, key);
             }
         }
-        const Threshold th = radix_threshold<NT, RB>(keys, valid, k, sm);
-        int gb = 0, eb = 0;
-        ordered_emit<NT, RB, 1>(keys, ids, valid, th,
-                                [&](int slot, uint32_t, int32_t id) { if (slot < k) out[slot] = id; }, sm, gb, eb);
+        block_minmax<kNT>(mn, mx, sm.cs);
+        const int m = sm.cs.cnt[2];
+        const Threshold th = smem_threshold<kNT>(
+            [&](int i, uint32_t &key) {
+                key = sm.ck[i];
+                return true;
+            },
+            m, k, mn, mx, sm.cs);
+        collect_smem<kNT>([&](int i) { return sm.ck[i]; }, [&](int i) { return sm.cid[i]; }, m, th, nullptr,
+                          sm.sid, sm.cs);
+        sort_emit<kNT>(sm.sid, k, k, out);
     }
     if (threadIdx.x == 0) a.tickets[q] = 0u;
 }
 
 // ---------------------------------------------------------------------------- launchers
 
-qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s) {
+template <bool SAMPLE>
+static qsa_status launch_row(const TopkArgs &a, cudaStream_t s) {
     if (a.bound <= 1024) {
-        topk_register_kernel<256, 1><<<a.nq, 256, 0, s>>>(a);
+        topk_row_kernel<1, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
+    } else if (a.bound <= 2048) {
+        topk_row_kernel<2, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
     } else if (a.bound <= 4096) {
-        topk_register_kernel<1024, 1><<<a.nq, 1024, 0, s>>>(a);
+        topk_row_kernel<4, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
     } else if (a.bound <= kRegisterCap) {
-        topk_register_kernel<1024, 2><<<a.nq, 1024, 0, s>>>(a);
+        topk_row_kernel<8, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
     } else {
-        return fail(QSA_ERR_UNSUPPORTED, "register path holds at most %d blocks per row (bound %d)",
-                    kRegisterCap, a.bound);
+        return fail(QSA_ERR_UNSUPPORTED, "%s path holds at most %d blocks per row (bound %d)",
+                    SAMPLE ? "sample" : "register", kRegisterCap, a.bound);
     }
-    return check_cuda(cudaGetLastError(), "topk_register_kernel launch");
+    return check_cuda(cudaGetLastError(), SAMPLE ? "topk_row_kernel<sample> launch" : "topk_row_kernel launch");
 }
+
+qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s) { return launch_row<false>(a, s); }
+
+qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) { return launch_row<true>(a, s); }
 
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s) {
     topk_radix_kernel<512><<<a.nq, 512, 0, s>>>(a, flagged_only ? 1 : 0);
     return check_cuda(cudaGetLastError(), "topk_radix_kernel launch");
-}
-
-qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) {
-    if (a.bound <= 4096) {
-        topk_sample_kernel<1024, 1><<<a.nq, 1024, 0, s>>>(a);
-    } else {
-        topk_sample_kernel<1024, 2><<<a.nq, 1024, 0, s>>>(a);
-    }
-    qsa_status st = check_cuda(cudaGetLastError(), "topk_sample_kernel launch");
-    if (st != QSA_OK) return st;
-    return launch_topk_radix(a, true, s);
 }
 
 SplitGeom split_geometry(int bound, int nq, int k, int maxch) {
@@ -430,10 +466,9 @@ SplitGeom split_geometry(int bound, int nq, int k, int maxch) {
 
 qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s) {
     if (g.chunk_len <= 0 || g.chunk_len > kSplitMaxChunk)
-        return fail(QSA_ERR_UNSUPPORTED, "split path: no chunk geometry fits (bound %d, k %d)",
-                    a.bound, a.k);
-    dim3 grid(g.nchunks, a.nq);
-    topk_split_kernel<256, kSplitSlots / 256><<<grid, 256, 0, s>>>(a, g.chunk_len);
+        return fail(QSA_ERR_UNSUPPORTED, "split path: no chunk geometry fits (bound %d, k %d)", a.bound, a.k);
+    const dim3 grid(g.nchunks, a.nq);
+    topk_split_kernel<<<grid, kNT, 0, s>>>(a, g.chunk_len);
     return check_cuda(cudaGetLastError(), "topk_split_kernel launch");
 }
 

@@ -25,7 +25,8 @@ PATH_AUTO, PATH_SPLIT, PATH_SAMPLE, PATH_REGISTER, PATH_RADIX = range(5)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SPLIT: "split", PATH_SAMPLE: "sample",
               PATH_REGISTER: "register", PATH_RADIX: "radix"}
 # flags word bits
-FLAG_NBLOCKS_CLAMPED, FLAG_WAIT_TIMEOUT, FLAG_INTERNAL = 0x1, 0x2, 0x4
+FLAG_NBLOCKS_CLAMPED, FLAG_WAIT_TIMEOUT, FLAG_INTERNAL, FLAG_SAMPLE_FALLBACK = 0x1, 0x2, 0x4, 0x8
+ERROR_FLAGS = FLAG_NBLOCKS_CLAMPED | FLAG_WAIT_TIMEOUT | FLAG_INTERNAL
 HEAD_DIM = 128
 MAX_K = 1024
 

@@ -44,7 +44,7 @@ def full_check(case, path=qsa.PATH_AUTO):
     ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
     ref_ids = oracle.select(ref, case.n_blocks, case.k)
     ids, sc, flags = run_select(case, path)
-    assert flags == 0, f"device flags {flags:#x}"
+    assert flags & qsa.ERROR_FLAGS == 0, f"device flags {flags:#x}"
     # scores are written exactly for b < n and left alone past it
     for qi, n in enumerate(case.n_blocks):
         assert np.isfinite(sc[qi, :n]).all()
@@ -104,7 +104,7 @@ def test_scorer_heads_and_dtypes(H, dtype):
     toks = inputs.ragged_tokens(7000 + H, nq, 300)
     case = inputs.make_case(7000 + H + 10 * dtype, nq, H, 300, dtype, toks, 8, active_blocks=300)
     sc, flags = gpu_scores(case)
-    assert flags == 0
+    assert flags & qsa.ERROR_FLAGS == 0
     ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
     parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
     for qi, n in enumerate(case.n_blocks):

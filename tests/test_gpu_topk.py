@@ -68,7 +68,7 @@ def test_topk_paths_match_oracle(path, kind, shape):
         raise
     want = oracle.select_f32(sc, nb, k)
     np.testing.assert_array_equal(ids, want)
-    assert flags == 0
+    assert flags & qsa.ERROR_FLAGS == 0
 
 
 @pytest.mark.parametrize("path", PATHS, ids=[qsa.PATH_NAMES[p] for p in PATHS])
@@ -86,7 +86,7 @@ def test_topk_edge_lengths(path):
             pytest.skip(e.reason)
         raise
     np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
-    assert flags == 0
+    assert flags & qsa.ERROR_FLAGS == 0
 
 
 @pytest.mark.parametrize("path", PATHS, ids=[qsa.PATH_NAMES[p] for p in PATHS])
@@ -160,3 +160,27 @@ def test_sample_fallback_is_taken_and_correct():
     nb = np.full(nq, 8192, dtype=np.int32)
     ids, flags, ws = run_topk(sc, nb, k, qsa.PATH_SAMPLE, active=8192)
     np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
+    assert flags & qsa.FLAG_SAMPLE_FALLBACK
+
+
+def test_sample_filter_is_used_on_continuous_scores():
+    """Continuous scores: the sampled bound keeps between k and 4,096 candidates for every query."""
+    nq, C, k = 64, 8192, 32
+    sc = inputs.normal_scores(6700, nq, C)
+    nb = np.full(nq, 8125, dtype=np.int32)
+    ids, flags, ws = run_topk(sc, nb, k, qsa.PATH_SAMPLE, active=8125)
+    np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
+    assert flags == 0
+
+
+@pytest.mark.parametrize("k", [1, 32, 100, 1024])
+def test_sample_few_candidates_falls_back(k):
+    """A spike per row: with k above the candidate count the filter falls back and stays exact."""
+    nq, C = 6, 8192
+    rng = np.random.default_rng(6800 + k)
+    sc = rng.integers(0, 3, size=(nq, C)).astype(np.float32)
+    sc[:, ::97] = 5.0
+    nb = np.array([8192, 8191, 5000, 4097, 4096, 2000], dtype=np.int32)
+    ids, flags, ws = run_topk(sc, nb, k, qsa.PATH_SAMPLE, active=8192)
+    np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
+    assert flags & qsa.ERROR_FLAGS == 0
