@@ -146,6 +146,30 @@ qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int3
                           void *ws, size_t ws_bytes, qsa_path path, qsa_stream stream);
 
 /*
+ * Block top-k for callers that cannot allocate device memory.  No passage of the
+ * source pages has a counterpart to this call; it exists for callers that may
+ * not call cudaMalloc where they select blocks (a fixed memory arena that must
+ * not grow, a plug-in given only its input and output buffers, a serving path
+ * where device allocation is forbidden).
+ *
+ * Same arguments, results and errors as qsa_block_topk, without ws / ws_bytes:
+ * the scratch is an 8 MiB array compiled into the library, held on every GPU
+ * that loads it until the process exits.  Sizes whose workspace
+ * (qsa_workspace_bytes(nq, max_blocks, k, 0)) exceeds 8 MiB are rejected with
+ * QSA_ERR_WORKSPACE and nothing is launched.  The call never allocates.
+ *
+ * The first call on each device looks up the scratch's device address (a CUDA
+ * runtime query, with that device current) and caches it; make that first call
+ * before any stream capture.  All calls share the one scratch array: the parts
+ * that must start at zero are cleared on `stream` at the start of every call,
+ * and calls that can overlap on the GPU (different streams or host threads)
+ * race with each other.  The device flags of these calls are not readable.
+ */
+qsa_status qsa_block_topk_static(const float *scores, int64_t scores_stride, const int32_t *n_blocks, int nq,
+                                 int max_blocks, int active_blocks, int k, int32_t *ids, qsa_path path,
+                                 qsa_stream stream);
+
+/*
  * Score then select, in one call.
  *
  * fused == 0 (chained): the scorer writes `scores` (required), then the top-k

@@ -31,7 +31,8 @@ HEAD_DIM = 128
 MAX_K = 1024
 
 EXPORTS = ("qsa_workspace_bytes", "qsa_workspace_init", "qsa_block_scores", "qsa_block_topk",
-           "qsa_select", "qsa_read_flags", "qsa_auto_path", "qsa_last_error", "qsa_version")
+           "qsa_block_topk_static", "qsa_select", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
+           "qsa_version")
 
 
 class QSAError(RuntimeError):
@@ -62,6 +63,8 @@ def load() -> ctypes.CDLL:
     lib.qsa_block_scores.restype = i32
     lib.qsa_block_topk.argtypes = [vp, i64, vp, i32, i32, i32, i32, vp, vp, sz, i32, vp]
     lib.qsa_block_topk.restype = i32
+    lib.qsa_block_topk_static.argtypes = [vp, i64, vp, i32, i32, i32, i32, vp, i32, vp]
+    lib.qsa_block_topk_static.restype = i32
     lib.qsa_select.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i64, i32, vp,
                                sz, i32, vp]
     lib.qsa_select.restype = i32
@@ -166,6 +169,25 @@ def block_topk(scores: torch.Tensor, n_blocks: torch.Tensor, k: int, ids: torch.
                             mb, active_blocks, k, _dptr(ids, "ids"), _dptr(ws, "ws"), ws.numel(),
                             path, _stream(stream))
     _check("qsa_block_topk", st)
+    return ids
+
+
+def block_topk_static(scores: torch.Tensor, n_blocks: torch.Tensor, k: int, ids: torch.Tensor,
+                      max_blocks: int | None = None, active_blocks: int = -1, path: int = PATH_AUTO,
+                      stream=None) -> torch.Tensor:
+    """block_topk without a workspace argument: the library's static scratch is used
+    (for callers that may not allocate device memory)."""
+    lib = load()
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be a 2-D fp32 tensor with unit inner stride")
+    if ids.dtype != torch.int32 or not ids.is_contiguous() or tuple(ids.shape) != (scores.shape[0], k):
+        raise ValueError("ids must be a contiguous int32 tensor [nq, k]")
+    _contig(n_blocks, "n_blocks")
+    nq = scores.shape[0]
+    mb = scores.shape[1] if max_blocks is None else max_blocks
+    st = lib.qsa_block_topk_static(_dptr(scores, "scores"), scores.stride(0), _dptr(n_blocks, "n_blocks"), nq,
+                                   mb, active_blocks, k, _dptr(ids, "ids"), path, _stream(stream))
+    _check("qsa_block_topk_static", st)
     return ids
 
 
