@@ -171,6 +171,23 @@ def timed_loop(torch, fn, steps, flush, stream, prime=True):
     return times
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest of every rank's value (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(ms_per_step_max: float, world: int) -> float:
+    """Whole-job figure for N replicas: each rank runs one call per step, so the job
+    completes `world` calls in the slowest rank's step time."""
+    return ms_per_step_max * 1e3 / world
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -349,17 +366,12 @@ def run_ours(args):
     t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream, prime=False)
     clocks = sampler.stop()
 
-    ms_main = statistics.mean(t_main)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_main], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_main = float(tt.item())
+    ms_main = max_over_ranks(statistics.mean(t_main), device=dev)
     if rank != 0:
         return 0
 
     peaks, peak_src = load_peaks()
-    us_main = ms_main * 1e3 / world          # whole job: world calls per step
+    us_main = job_us_per_call(ms_main, world)
     us_score = statistics.median(t_score) * 1e3
     us_topk = statistics.median(t_topk) * 1e3
     flops = 2.0 * case.nq * case.n_heads * 128 * n

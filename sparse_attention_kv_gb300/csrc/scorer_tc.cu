@@ -36,8 +36,10 @@ namespace qsa {
 namespace {
 
 constexpr int kBM = 128;       // KV blocks per tile (MMA M = TMEM lanes)
-constexpr int kThreads = 576;  // 18 warps: TMA, MMA, 16 epilogue
-constexpr int kEpi = 512;      // epilogue threads
+constexpr int kEpiParts = 4;                  // epilogue warps per TMEM lane quarter
+constexpr int kEpi = 128 * kEpiParts;         // epilogue threads
+constexpr int kThreads = 64 + kEpi;           // + one TMA warp and one MMA warp
+constexpr int kMaxChunks = (16 + kEpiParts - 1) / kEpiParts;  // 16-column chunks per thread
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
 
 template <bool F32>
@@ -75,7 +77,7 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort;
     int maxn;
-    int pad;
+    int epi_ok[2];
     __align__(16) float w[256];
     int nb[256];
 };
@@ -251,6 +253,9 @@ __device__ __forceinline__ float head_sum(const float *w, const uint32_t *acc) {
     }
 }
 
+// Named barrier 1 over the epilogue warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ct.done, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ct.tfull[b], 1);
-            mbar_init(&ct.tempty[b], kEpi);
+            mbar_init(&ct.tempty[b], kEpi / 32);
         }
         ct.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -445,16 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(&ct.done, 0);
         }
     } else {
-        // ---------------- epilogue: warps 2..17, one accumulator row per thread.
-        // The four warps of a TMEM lane quarter (warp % 4) split the tile's
-        // 16-column chunks (16/H queries each) into four parts.
+        // ---------------- epilogue: warps 2.., one accumulator row per thread.
+        // The kEpiParts warps of a TMEM lane quarter (warp % 4) split the tile's
+        // 16-column chunks (16/H queries each) between them.
         const int et = tid - 64;                 // 0..511
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int part = (warp - 2) >> 2;        // 0..3
+        const int part = (warp - 2) >> 2;        // 0..kEpiParts-1
         const int row = quarter * 32 + lane;
         const int nchunk = (qv * H + 15) / 16;   // <= 16
-        const int c_begin = part * nchunk / 4;
-        const int c_end = (part + 1) * nchunk / 4;
+        const int c_begin = part * nchunk / kEpiParts;
+        const int c_end = (part + 1) * nchunk / kEpiParts;
         bool ok = true;
         if constexpr (F32) {
             ok = __all_sync(0xffffffffu, mbar_wait(&ct.bfull, 0, abort_flag));
@@ -473,23 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = i & 1;
             const uint32_t tph = (uint32_t)(i >> 1) & 1u;
-            // warp-uniform: tcgen05.ld below is a warp-collective instruction
-            if (!__all_sync(0xffffffffu, mbar_wait(&ct.tfull[b], tph, abort_flag))) break;
+            // One thread waits for the accumulator; the other epilogue threads
+            // block on a hardware barrier, which takes no issue slots.
+            if (et == 0) ct.epi_ok[b] = mbar_wait(&ct.tfull[b], tph, abort_flag) ? 1 : 0;
+            epilogue_sync();
+            if (!ct.epi_ok[b]) break;   // uniform across the epilogue
             tc_fence_after();
             const int blk = (t_begin + i) * kBM + row;
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * buf_cols);
             // every column chunk of this thread's part in flight at once, one wait
-            const int nc = c_end - c_begin;   // <= 4
-            uint32_t v[4][16];
+            const int nc = c_end - c_begin;   // <= kMaxChunks
+            uint32_t v[kMaxChunks][16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < kMaxChunks; ++cc)
                 if (cc < nc) tmem_ld16_nowait(taddr + (uint32_t)((c_begin + cc) * 16), v[cc]);
             tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < kMaxChunks; ++cc)
                 if (cc < nc) reg_fence(v[cc]);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < kMaxChunks; ++cc) {
                 if (cc < nc) {
 #pragma unroll
                     for (int jj = 0; jj < 16 / H; ++jj) {
@@ -502,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&ct.tempty[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ct.tempty[b]);
         }
     }
     __syncthreads();
