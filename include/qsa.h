@@ -174,10 +174,14 @@ qsa_status qsa_block_topk_static(const float *scores, int64_t scores_stride, con
  *
  * fused == 0 (chained): the scorer writes `scores` (required), then the top-k
  *   reads them; both are the calls above.
- * fused != 0: the scorer's epilogue keeps each CTA's block range on chip, picks
- *   that range's candidates and the last CTA of a query group merges them; the
- *   scores never go to HBM.  `scores` may be NULL; when given, it also receives
- *   the scores (bit-identical to the chained scorer's).
+ * fused != 0: one kernel.  The scorer's epilogue keeps each CTA's block range of
+ *   scores on chip, one warp per query picks that range's k candidates, and the
+ *   last CTA of a query group to finish merges them (no CTA waits for another);
+ *   the scores never go to HBM.  `scores` may be NULL; when given, it also
+ *   receives the scores (the same values the chained scorer writes).  `path`
+ *   must be QSA_PATH_AUTO.  Shapes whose per-CTA scores or candidates do not fit
+ *   on chip (large k, very long contexts) return QSA_ERR_UNSUPPORTED; use the
+ *   chained form for those.
  * Arguments as in qsa_block_scores / qsa_block_topk; ws must hold
  * qsa_workspace_bytes(nq, max_blocks, k, fused) bytes.
  */

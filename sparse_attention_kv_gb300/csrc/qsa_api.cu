@@ -241,8 +241,35 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
     if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
     st = check_ws(ws, ws_bytes, nq, max_blocks, k);
     if (st != QSA_OK) return st;
-    if (fused) return fail(QSA_ERR_UNSUPPORTED, "fused score-then-select is not built yet");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fused) {
+        if (path != QSA_PATH_AUTO)
+            return fail(QSA_ERR_UNSUPPORTED, "fused score-then-select has no top-k path to force (got %d)", (int)path);
+        const WsLayout L = ws_layout(nq, max_blocks, k);
+        char *base = static_cast<char *>(ws);
+        ScorerArgs a{};
+        a.q = q;
+        a.w = w;
+        a.kblk = kblk;
+        a.dt = dt;
+        a.n_blocks = n_blocks;
+        a.nq = nq;
+        a.n_heads = n_heads;
+        a.max_blocks = max_blocks;
+        a.bound = effective_bound(max_blocks, active_blocks);
+        a.scores = scores;   // may be null
+        a.stride = scores_stride;
+        a.flags = reinterpret_cast<uint32_t *>(base + L.flags);
+        a.fused = true;
+        a.ids = ids;
+        a.k = k;
+        a.tickets = reinterpret_cast<uint32_t *>(base + L.tickets);
+        // 8 bytes per candidate fit in the two 4-byte candidate arrays, which are adjacent
+        static_assert(sizeof(uint64_t) == 2 * sizeof(uint32_t), "packed candidate size");
+        a.cand = reinterpret_cast<uint64_t *>(base + L.ckeys);
+        a.maxch = L.maxch;
+        return launch_scorer(a, s);
+    }
     st = qsa_block_scores(q, w, kblk, dt, n_blocks, nq, n_heads, head_dim, max_blocks, active_blocks,
                           scores, scores_stride, ws, ws_bytes, stream);
     if (st != QSA_OK) return st;

@@ -342,4 +342,221 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t (&x)[8], int r) {
     return res;
 }
 
+
+// ---------------------------------------------------------------------------
+// One warp selecting over a list held in shared memory (no block barriers).
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Warp-wide min / max of 32- and 64-bit keys.
+__device__ __forceinline__ uint32_t warp_min(uint32_t x) { return __reduce_min_sync(kFull, x); }
+__device__ __forceinline__ uint32_t warp_max(uint32_t x) { return __reduce_max_sync(kFull, x); }
+__device__ __forceinline__ uint64_t warp_min(uint64_t x) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const uint64_t o = __shfl_xor_sync(kFull, x, d);
+        x = o < x ? o : x;
+    }
+    return x;
+}
+__device__ __forceinline__ uint64_t warp_max(uint64_t x) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const uint64_t o = __shfl_xor_sync(kFull, x, d);
+        x = o > x ? o : x;
+    }
+    return x;
+}
+__device__ __forceinline__ int key_clz(uint32_t x) { return __clz(x); }
+__device__ __forceinline__ int key_clz(uint64_t x) { return __clzll(x); }
+
+// One warp: emit, in list order, every entry with key > T and the first `budget`
+// entries with key == T; stops once k entries are out.  emit(pos, i) as below.
+template <typename K, typename KeyAt, typename Emit>
+__device__ __forceinline__ void warp_emit_ordered(KeyAt &&key_at, int n, int k, K T, int budget, Emit &&emit) {
+    const int lane = threadIdx.x & 31;
+    int taken = 0, ties = 0;
+    for (int base = 0; base < n && taken < k; base += 32) {
+        const int i = base + lane;
+        const K key = i < n ? key_at(i) : K(0);
+        const bool gt = i < n && key > T;
+        const bool eq = i < n && key == T;
+        const unsigned eqm = __ballot_sync(kFull, eq);
+        const bool take = gt || (eq && ties + __popc(eqm & lanemask_lt()) < budget);
+        const unsigned tm = __ballot_sync(kFull, take);
+        if (take) emit(taken + __popc(tm & lanemask_lt()), i);
+        taken += __popc(tm);
+        ties += __popc(eqm);
+    }
+}
+
+// The k selected entries of a list i < n (key_at(i) gives a 32- or 64-bit key),
+// in list order: every key > T plus, of the keys == T, the first `budget` in list
+// order (T = the k-th largest key).  When the list is in ascending block-id order
+// the result is the reference selection in ascending id order.  emit(pos, i) is
+// called for each selected entry with its output slot pos (0..min(n,k)-1).
+// hist: this warp's 256-word shared histogram (zero on entry, left zero).
+// All 32 lanes call; no block-wide barrier is used.
+template <typename KeyAt, typename Emit>
+__device__ void warp_select(KeyAt &&key_at, int n, int k, uint32_t *hist, Emit &&emit) {
+    using K = decltype(key_at(0));
+    constexpr int kBits = 8 * sizeof(K);
+    const int lane = threadIdx.x & 31;
+    if (n <= k) {   // everything is selected
+        for (int i = lane; i < n; i += 32) emit(i, i);
+        return;
+    }
+    K mn = ~K(0), mx = K(0);
+    for (int i = lane; i < n; i += 32) {
+        const K key = key_at(i);
+        mn = min(mn, key);
+        mx = max(mx, key);
+    }
+    mn = warp_min(mn);
+    mx = warp_max(mx);
+    int hi = kBits - key_clz(mn ^ mx);
+    K prefix = hi == kBits ? K(0) : (mx & ~((K(1) << hi) - K(1)));
+    int remaining = k;
+    while (hi > 0) {
+        const int lo = hi > 8 ? hi - 8 : 0;
+        const int nbins = 1 << (hi - lo);
+        for (int i = lane; i < n; i += 32) {
+            const K key = key_at(i);
+            if (hi == kBits || (key >> hi) == (prefix >> hi))
+                atomicAdd(&hist[static_cast<uint32_t>(key >> lo) & (uint32_t)(nbins - 1)], 1u);
+        }
+        __syncwarp();
+        uint32_t c[8];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int b = nbins - 1 - 8 * lane - j;
+            c[j] = 0u;
+            if (b >= 0) {
+                c[j] = hist[b];
+                hist[b] = 0u;
+            }
+            sum += (int)c[j];
+        }
+        const int incl = warp_incl_scan(sum);
+        int run = incl - sum;
+        int digit = 0, above = 0;
+        const bool mine = run < remaining && remaining <= incl;
+        if (mine) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (run + (int)c[j] >= remaining) {
+                    digit = nbins - 1 - 8 * lane - j;
+                    above = run;
+                    break;
+                }
+                run += (int)c[j];
+            }
+        }
+        const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+        digit = __shfl_sync(kFull, digit, src);
+        above = __shfl_sync(kFull, above, src);
+        remaining -= above;
+        prefix |= static_cast<K>(digit) << lo;
+        hi = lo;
+        __syncwarp();
+    }
+    warp_emit_ordered(key_at, n, k, prefix, remaining, emit);
+}
+
+
+// ---------------------------------------------------------------------------
+// Packed candidates and warp sorting networks.
+//
+// A candidate (key, block id) packs into (key << 32) | ~id.  Block ids are
+// distinct and non-negative, so packed values are distinct, never 0, and a larger
+// packed value is a larger key or, on equal keys, a lower block id: the order in
+// which the selection takes blocks.
+
+__device__ __forceinline__ uint64_t pack_cand(uint32_t key, int32_t id) {
+    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~id);
+}
+__device__ __forceinline__ uint32_t cand_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ int32_t cand_id(uint64_t c) { return ~static_cast<int32_t>(static_cast<uint32_t>(c)); }
+
+// Bitonic sort of 64 values held two per lane (element 2 * lane + s is v_s),
+// descending: afterwards element r is the (r+1)-th largest.  21 compare-exchange
+// steps, 15 of them across lanes.
+template <typename T>
+__device__ __forceinline__ void warp_sort64_desc(T &v0, T &v1) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 64; size <<= 1) {
+        const bool desc = ((2 * lane) & size) == 0;
+#pragma unroll
+        for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+            if (stride == 1) {
+                const T hi = v0 > v1 ? v0 : v1, lo = v0 > v1 ? v1 : v0;
+                v0 = desc ? hi : lo;
+                v1 = desc ? lo : hi;
+            } else {
+                const int d = stride >> 1;   // partner lane distance
+                const bool keep_max = ((lane & d) == 0) == desc;
+                const T o0 = __shfl_xor_sync(kFull, v0, d), o1 = __shfl_xor_sync(kFull, v1, d);
+                v0 = keep_max ? (v0 > o0 ? v0 : o0) : (v0 > o0 ? o0 : v0);
+                v1 = keep_max ? (v1 > o1 ? v1 : o1) : (v1 > o1 ? o1 : v1);
+            }
+        }
+    }
+}
+
+// Bitonic sort of 32 values, one per lane, ascending by lane.
+template <typename T>
+__device__ __forceinline__ void warp_sort32_asc(T &v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+        const bool asc = (lane & size) == 0;
+#pragma unroll
+        for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+            const T o = __shfl_xor_sync(kFull, v, stride);
+            const bool keep_min = ((lane & stride) == 0) == asc;
+            v = keep_min ? (v < o ? v : o) : (v < o ? o : v);
+        }
+    }
+}
+
+// The k-th largest (1 <= k <= 32) of the 64 values held two per lane: a lower
+// bound of a list's k-th largest key when each lane holds the two largest keys of
+// its own share of the list (distinct entries; 0 where a share has fewer than
+// two), since then k distinct entries reach it.
+__device__ __forceinline__ uint32_t warp_bound_from_top2(uint32_t m1, uint32_t m2, int k) {
+    warp_sort64_desc(m1, m2);
+    const int r = k - 1;
+    return __shfl_sync(kFull, (r & 1) ? m2 : m1, r >> 1);
+}
+
+// The top k of m <= 64 distinct packed candidates buf[0..m) (k <= m): emit(r, c)
+// for the candidate c of rank r < k (rank 0 the largest).  Each lane ranks
+// entries lane and lane + 32 against all m by shared-memory broadcast reads, so
+// there is no shuffle chain.  buf needs 16-byte alignment and room for 64.
+template <typename Emit>
+__device__ __forceinline__ void warp_rank_top(uint64_t *buf, int m, int k, Emit &&emit) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && (m & 1)) buf[m] = 0ull;   // pad to pairs: 0 is below every candidate
+    __syncwarp();
+    const uint64_t v0 = lane < m ? buf[lane] : 0ull;
+    const uint64_t v1 = lane + 32 < m ? buf[lane + 32] : 0ull;
+    int r0 = 0, r1 = 0;
+    const ulonglong2 *b2 = reinterpret_cast<const ulonglong2 *>(buf);
+#pragma unroll 4
+    for (int j = 0; j < (m + 1) >> 1; ++j) {
+        const ulonglong2 pr = b2[j];
+        r0 += (pr.x > v0) + (pr.y > v0);
+        r1 += (pr.x > v1) + (pr.y > v1);
+    }
+    if (lane < m && r0 < k) emit(r0, v0);
+    if (lane + 32 < m && r1 < k) emit(r1, v1);
+    __syncwarp();
+}
+
 }  // namespace qsa

@@ -83,6 +83,13 @@ struct ScorerArgs {
     float *scores;
     int64_t stride;
     uint32_t *flags;
+    // fused score-then-select (fused != 0): scores may be null
+    bool fused;
+    int32_t *ids;
+    int k;
+    uint32_t *tickets;
+    uint64_t *cand;   // [nq][maxch][k] packed candidates; spans the ckeys and cids regions
+    int maxch;
 };
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);
 

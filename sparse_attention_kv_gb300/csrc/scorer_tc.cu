@@ -30,6 +30,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "qsa_device.cuh"
 #include "qsa_internal.h"
 
 namespace qsa {
@@ -58,17 +59,21 @@ struct Cfg<true> {  // fp32 -> kind::tf32, three-term split
 // One 128-byte swizzle atom of a tile holds rows x 128 bytes (kEPA elements of K).
 constexpr int kAtomA = kBM * 128;  // 16 KB
 
-template <bool F32>
+// The fused kernel keeps each CTA's scores on chip (kSbuf bytes) and gives each
+// epilogue warp a 256-bin histogram; it pays for them with fewer kblk stages.
+template <bool F32, bool FUSED>
 struct Layout {
     using C = Cfg<F32>;
+    static constexpr int kStages = (FUSED && !F32) ? 2 : C::kStages;
     static constexpr int kB = C::kAtoms * C::kMaxBN * 128;
     static constexpr int kAStage = C::kAtoms * kAtomA;
     static constexpr int offB = 0;
     static constexpr int offBlo = offB + kB;
     static constexpr int offA = offBlo + (F32 ? kB : 0);
-    static constexpr int offAlo = offA + C::kStages * kAStage;
-    static constexpr int offCtrl = offAlo + (F32 ? C::kStages * kAStage : 0);
+    static constexpr int offAlo = offA + kStages * kAStage;
+    static constexpr int offCtrl = offAlo + (F32 ? kStages * kAStage : 0);
 };
+constexpr int kHistBytes = (kEpi / 32) * 256 * 4;   // one 256-bin histogram per epilogue warp
 
 struct Ctrl {
     uint64_t full[4], empty[4], split[4];
@@ -78,12 +83,19 @@ struct Ctrl {
     int abort;
     int maxn;
     int epi_ok[2];
+    int last;
     __align__(16) float w[256];
     int nb[256];
 };
 
-template <bool F32>
-constexpr int smem_bytes() { return Layout<F32>::offCtrl + (int)sizeof(Ctrl) + 1024; }
+template <bool F32, bool FUSED>
+constexpr int sbuf_bytes() {
+    return FUSED ? (227 * 1024 - 1024 - Layout<F32, FUSED>::offCtrl - (int)sizeof(Ctrl) - kHistBytes) / 1024 * 1024 : 0;
+}
+template <bool F32, bool FUSED>
+constexpr int smem_bytes() {
+    return Layout<F32, FUSED>::offCtrl + (int)sizeof(Ctrl) + (FUSED ? kHistBytes + sbuf_bytes<F32, FUSED>() : 0) + 1024;
+}
 
 struct KParams {
     const float *w;
@@ -92,6 +104,13 @@ struct KParams {
     int64_t stride;
     uint32_t *flags;
     int nq, bound, qg, bn, tiles_per_cta, tiles_total, tmem_cols;
+    // fused score-then-select only
+    int32_t *ids;
+    int k;
+    uint32_t *tickets;
+    uint64_t *cand;    // [nq][maxch][k] packed candidates
+    int maxch;
+    int sb_stride;     // scores per query in the on-chip buffer (tiles_per_cta * 128)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -293,14 +312,315 @@ __device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes,
     }
 }
 
+// ---------------------------------------------------------------- fused select
+
+// Stage A of one query on one CTA, fast form (k <= 32): the exact top-k of the
+// CTA's n > k scores of the query (row[0..n), block ids lo + i), written to
+// dst[0..k) as packed candidates in descending order.  Each lane keeps the two
+// largest keys of its share, the k-th largest of those 64 bounds the answer from
+// below, the keys at or above it (about k + 4 on continuous scores) are gathered
+// into buf at offsets from one warp scan of the lanes' counts, and their exact
+// ranks pick the top k.  Rows of up to 32 * 4 * NV scores are held in registers
+// (one read of shared memory); longer rows are read three times.  Returns false,
+// having written nothing, when more than 64 keys reach the bound (heavy ties).
+template <int NV>
+__device__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
+    const int lane = threadIdx.x & 31;
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);   // rows start on 512-byte boundaries
+    uint32_t key[NV][4];
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        const int v = lane + 32 * t;
+        const float4 f = 4 * v < n ? r4[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) key[t][c] = 4 * v + c < n ? score_key(e[c]) : 0u;
+    }
+    uint32_t a1[4] = {0u, 0u, 0u, 0u}, a2[4] = {0u, 0u, 0u, 0u};   // one top-2 per component
+#pragma unroll
+    for (int t = 0; t < NV; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            a2[c] = max(a2[c], min(a1[c], key[t][c]));
+            a1[c] = max(a1[c], key[t][c]);
+        }
+    uint32_t m1 = a1[0], m2 = a2[0];
+#pragma unroll
+    for (int c = 1; c < 4; ++c) {   // top-2 of two top-2 pairs
+        m2 = max(min(m1, a1[c]), max(m2, a2[c]));
+        m1 = max(m1, a1[c]);
+    }
+    // absent entries have key 0; a zero bound keeps them, which the count below excludes
+    const uint32_t lb = warp_bound_from_top2(m1, m2, k);
+    int nk = 0;
+#pragma unroll
+    for (int t = 0; t < NV; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) nk += 4 * (lane + 32 * t) + c < n && key[t][c] >= lb;
+    const int incl = warp_incl_scan(nk);
+    const int m = __shfl_sync(kFull, incl, 31);
+    if (m > 64) return false;
+    int pos = incl - nk;
+#pragma unroll
+    for (int t = 0; t < NV; ++t)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int i = 4 * (lane + 32 * t) + c;
+            if (i < n && key[t][c] >= lb) buf[pos++] = pack_cand(key[t][c], lo + i);
+        }
+    __syncwarp();
+    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
+    return true;
+}
+
+__device__ bool stage_a_smem(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
+    const int lane = threadIdx.x & 31;
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+    const int n4 = (n + 3) >> 2;
+    uint32_t a1[4] = {0u, 0u, 0u, 0u}, a2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 2
+    for (int v = lane; v < n4; v += 32) {
+        const float4 f = r4[v];
+        const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t key = 4 * v + c < n ? score_key(e[c]) : 0u;
+            a2[c] = max(a2[c], min(a1[c], key));
+            a1[c] = max(a1[c], key);
+        }
+    }
+    uint32_t m1 = a1[0], m2 = a2[0];
+#pragma unroll
+    for (int c = 1; c < 4; ++c) {
+        m2 = max(min(m1, a1[c]), max(m2, a2[c]));
+        m1 = max(m1, a1[c]);
+    }
+    const uint32_t lb = warp_bound_from_top2(m1, m2, k);
+    int nk = 0;
+#pragma unroll 2
+    for (int v = lane; v < n4; v += 32) {
+        const float4 f = r4[v];
+        const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) nk += 4 * v + c < n && score_key(e[c]) >= lb;
+    }
+    const int incl = warp_incl_scan(nk);
+    const int m = __shfl_sync(kFull, incl, 31);
+    if (m > 64) return false;
+    int pos = incl - nk;
+    for (int v = lane; v < n4; v += 32) {
+        const float4 f = r4[v];
+        const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t key = score_key(e[c]);
+            if (4 * v + c < n && key >= lb) buf[pos++] = pack_cand(key, lo + 4 * v + c);
+        }
+    }
+    __syncwarp();
+    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
+    return true;
+}
+
+// Stage B of one query, fast form (k <= 32).  list holds the query's chunks, chunk
+// c at list[c * kc], its cnt_c = min(kc, max(0, n - c * S)) candidates in
+// descending order.  The keys of 64 sampled heads (rank e / nch of chunk e % nch,
+// e < 64) bound the k-th largest key from below; the candidates at or above it are
+// a prefix of each chunk, gathered into buf and ranked exactly.  The selected ids
+// go to out[0..k) ascending.  Returns false, having written nothing, when more
+// than 64 candidates reach the bound.
+__device__ bool stage_b_fast(const uint64_t *list, int nch, int kc, int S, int n, int k, uint64_t *buf, int32_t *sid,
+                             int32_t *out) {
+    const int lane = threadIdx.x & 31;
+    uint32_t x[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int e = 2 * lane + s, c = e % nch, rr = e / nch;
+        x[s] = rr < min(kc, n - c * S) ? cand_key(list[c * kc + rr]) : 0u;
+    }
+    const uint32_t lb = warp_bound_from_top2(x[0], x[1], k);
+    if (lb == 0u) return false;   // fewer than k heads: no bound
+    int m = 0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+        const int c = c0 + lane;
+        int p = 0;
+        if (c < nch) {
+            const int cc = min(kc, n - c * S);
+            while (p < cc && cand_key(list[c * kc + p]) >= lb) ++p;
+        }
+        const int incl = warp_incl_scan(p);
+        const int off = m + incl - p;
+        for (int i = 0; i < p && off + i < 64; ++i) buf[off + i] = list[c * kc + i];
+        m += __shfl_sync(kFull, incl, 31);
+    }
+    __syncwarp();
+    if (m > 64) return false;
+    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { sid[r] = cand_id(c); });
+    int32_t id = lane < k ? sid[lane] : 0x7fffffff;
+    warp_sort32_asc(id);
+    if (lane < k) out[lane] = id;
+    __syncwarp();
+    return true;
+}
+
+// The selection tail of the fused kernel.  Stage A: each epilogue warp takes the
+// queries j = warp, warp + 16, ... of the group and writes the top min(n_loc, k)
+// of this CTA's blocks of the query to cand[q][chunk] (descending for k <= 32,
+// else in block order).  The CTA then takes a ticket; the last CTA of the group
+// runs stage B: it loads every chunk's candidates of every query into shared
+// memory (a chunk c holds min(k, max(0, n - c * S)) of them, S = blocks per CTA,
+// so the lists need no counts and concatenate without gaps) and each warp
+// selects its queries' k blocks from them.  A query's selection restricted to one
+// CTA's range of blocks is a prefix of that range's selection order, so every
+// selected block is among its CTA's candidates (the split of Strata PR #3987,
+// section "Approach"), and the result equals selecting from the whole row.
+__device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbuf, uint32_t *hist, int q0, int qv,
+                                          int t_begin, int ntiles) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ew = warp - 2;   // epilogue warp index; the TMA and MMA warps only join the barriers
+    constexpr int nw = kEpi / 32;
+    const int c = blockIdx.x, nch = gridDim.x, g = blockIdx.y;
+    // the parameters live in memory that any store here could alias: read them once
+    const int k = p.k, maxch = p.maxch, sb_stride = p.sb_stride;
+    uint64_t *const __restrict__ cand = p.cand;
+    int32_t *const __restrict__ ids = p.ids;
+    uint32_t *const tickets = p.tickets;
+    // per-warp scratch (1 KB): the fast forms' 64-entry buffer and id slots, or the fallbacks' 256-bin histogram (zero on entry to warp_select)
+    uint32_t *h = hist + (ew > 0 ? ew : 0) * 256;
+    uint64_t *buf = reinterpret_cast<uint64_t *>(h);
+    int32_t *sid = reinterpret_cast<int32_t *>(h + 160);
+    const bool fast = k <= 32;
+    if (ew >= 0) {
+        for (int i = lane; i < 256; i += 32) h[i] = 0u;
+        __syncwarp();
+        const int lo = t_begin * kBM;
+        for (int j = ew; j < qv; j += nw) {
+            const int q = q0 + j;
+            const int n = ct.nb[j];
+            if (n <= k) continue;   // stage B emits 0..n-1
+            const int nloc = max(0, min(ntiles * kBM, n - lo));
+            uint64_t *dst = cand + ((size_t)q * maxch + c) * k;
+            const float *row = sbuf + (size_t)j * sb_stride;   // this CTA's blocks of query j
+            if (nloc <= k) {
+                for (int i = lane; i < nloc; i += 32) dst[i] = pack_cand(score_key(row[i]), lo + i);
+                if (fast) {   // descending, like the other chunks
+                    __syncwarp();
+                    uint64_t v = lane < nloc ? ~dst[lane] : ~0ull;
+                    __syncwarp();
+                    warp_sort32_asc(v);
+                    if (lane < nloc) dst[lane] = ~v;
+                }
+                continue;
+            }
+            if (fast) {
+                bool ok;
+                if (nloc <= 128) ok = stage_a_regs<1>(row, nloc, k, lo, buf, dst);
+                else if (nloc <= 256) ok = stage_a_regs<2>(row, nloc, k, lo, buf, dst);
+                else if (nloc <= 512) ok = stage_a_regs<4>(row, nloc, k, lo, buf, dst);
+                else if (nloc <= 1024) ok = stage_a_regs<8>(row, nloc, k, lo, buf, dst);
+                else ok = stage_a_smem(row, nloc, k, lo, buf, dst);
+                if (ok) continue;
+            }
+            for (int i = lane; i < 256; i += 32) h[i] = 0u;
+            __syncwarp();
+            warp_select([&](int i) { return score_key(row[i]); }, nloc, k, h,
+                        [&](int pos, int i) { dst[pos] = pack_cand(score_key(row[i]), lo + i); });
+            __syncwarp();
+            if (fast) {   // re-sort descending
+                uint64_t v = lane < k ? ~dst[lane] : ~0ull;
+                __syncwarp();
+                warp_sort32_asc(v);
+                if (lane < k) dst[lane] = ~v;
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) ct.last = atomicAdd(&tickets[g], 1u) == (unsigned)nch - 1u;
+    __syncthreads();
+    if (!ct.last) return;
+    if (tid == 0) __threadfence();
+    __syncthreads();
+    // every candidate of the group into shared memory: query j's list at lists[j * per],
+    // a warp per (query, chunk) row, a lane per candidate, kR rows in flight
+    const int S = sb_stride;             // blocks per CTA
+    const int kc = min(k, S);            // candidates of a full chunk
+    const int per = nch * kc;
+    uint64_t *lists = reinterpret_cast<uint64_t *>(sbuf);
+    {
+        constexpr int kWarps = kThreads / 32, kR = 8;
+        const int rows = qv * nch;
+        for (int i0 = 0; i0 < kc; i0 += 32) {
+            const int i = i0 + lane;
+            for (int r0 = warp; r0 < rows; r0 += kWarps * kR) {
+                uint64_t v[kR];
+                int at[kR];
+#pragma unroll
+                for (int u = 0; u < kR; ++u) {
+                    const int r = r0 + u * kWarps;
+                    at[u] = -1;
+                    v[u] = 0ull;
+                    if (r < rows) {
+                        const int j = r / nch, cc = r - j * nch;
+                        const int n = ct.nb[j];
+                        if (n > k && i < min(kc, n - cc * S)) {
+                            v[u] = __ldcg(cand + ((size_t)(q0 + j) * maxch + cc) * k + i);
+                            at[u] = j * per + cc * kc + i;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kR; ++u)
+                    if (at[u] >= 0) lists[at[u]] = v[u];
+            }
+        }
+    }
+    __syncthreads();
+    if (ew >= 0) {
+        for (int j = ew; j < qv; j += nw) {
+            const int q = q0 + j;
+            const int n = ct.nb[j];
+            int32_t *out = ids + (size_t)q * k;
+            if (n <= k) {
+                for (int i = lane; i < k; i += 32) out[i] = i < n ? i : -1;
+                continue;
+            }
+            const int full = n / S;
+            const int L = full * kc + min(kc, n - full * S);   // n <= nch * S
+            const uint64_t *list = lists + (size_t)j * per;
+            if (fast) {
+                if (L > k && stage_b_fast(list, nch, kc, S, n, k, buf, sid, out)) continue;
+                // exact 64-bit selection (no ties: packed values are distinct), then ids ascending
+                for (int i = lane; i < 256; i += 32) h[i] = 0u;
+                __syncwarp();
+                warp_select([&](int i) { return list[i]; }, L, k, h, [&](int pos, int i) { out[pos] = cand_id(list[i]); });
+                __syncwarp();
+                int32_t id = lane < min(L, k) ? out[lane] : 0x7fffffff;
+                __syncwarp();
+                warp_sort32_asc(id);
+                if (lane < k) out[lane] = lane < L ? id : -1;
+                __syncwarp();
+                continue;
+            }
+            for (int i = lane; i < 256; i += 32) h[i] = 0u;
+            __syncwarp();
+            warp_select([&](int i) { return cand_key(list[i]); }, L, k, h,
+                        [&](int pos, int i) { out[pos] = cand_id(list[i]); });
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (tid == 0) tickets[g] = 0u;
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <bool F32, int H>
+template <bool F32, int H, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     scorer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                      const KParams p) {
     using C = Cfg<F32>;
-    using L = Layout<F32>;
+    using L = Layout<F32, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sB = smem + L::offB;
@@ -309,6 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sAlo = smem + L::offAlo;
     Ctrl &ct = *reinterpret_cast<Ctrl *>(smem + L::offCtrl);
     volatile int *abort_flag = &ct.abort;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + L::offCtrl + sizeof(Ctrl));       // FUSED only
+    float *sbuf = reinterpret_cast<float *>(smem + L::offCtrl + sizeof(Ctrl) + kHistBytes);  // FUSED only
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.y;
@@ -347,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&ct.bfull, (uint32_t)(C::kAtoms * bn * 128));
         for (int a = 0; a < C::kAtoms; ++a)
             tma_load_2d(sB + a * bn * 128, &tm_q, &ct.bfull, a * C::kEPA, q0 * H);
-        const int pre = min(C::kStages, t_cap);
+        const int pre = min(L::kStages, t_cap);
         for (int i = 0; i < pre; ++i) {
             mbar_expect_tx(&ct.full[i], (uint32_t)(C::kAtoms * kAtomA));
             for (int a = 0; a < C::kAtoms; ++a)
@@ -374,13 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles_g = (ct.maxn + kBM - 1) / kBM;
     const int ntiles = min(t_begin + p.tiles_per_cta, ntiles_g) - t_begin;
     if (ntiles <= 0) {
-        if (tid == 0) {   // nothing to compute: let the early loads land before exiting
+        if (tid == 0) {   // nothing to compute: let the early loads land
             for (int j = 0; j < issued; ++j) mbar_drain(&ct.full[j], 0);
             mbar_drain(&ct.bfull, 0);
         }
-        return;
-    }
-
+        if constexpr (!FUSED) return;
+    } else {
     if (warp == 1) {
         tmem_alloc(&ct.tmem_base, (uint32_t)p.tmem_cols);
         tmem_relinquish();
@@ -395,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- producer (tiles after the early ones)
             for (int i = issued; i < ntiles; ++i) {
-                const int s = i % C::kStages;
-                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                const int s = i % L::kStages;
+                const uint32_t ph = (uint32_t)(i / L::kStages) & 1u;
                 if (!mbar_wait(&ct.empty[s], ph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&ct.full[s], (uint32_t)(C::kAtoms * kAtomA));
                 const int row = (t_begin + i) * kBM;
@@ -405,8 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++issued;
             }
             // drain: the latest load of every stage and the query tile
-            for (int j = max(0, issued - C::kStages); j < issued; ++j)
-                mbar_drain(&ct.full[j % C::kStages], (uint32_t)(j / C::kStages) & 1u);
+            for (int j = max(0, issued - L::kStages); j < issued; ++j)
+                mbar_drain(&ct.full[j % L::kStages], (uint32_t)(j / L::kStages) & 1u);
             mbar_drain(&ct.bfull, 0);
         }
     } else if (warp == 1) {
@@ -416,8 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(F32 ? &ct.bsplit : &ct.bfull, 0, abort_flag);
             tc_fence_after();
             for (int i = 0; ok && i < ntiles; ++i) {
-                const int s = i % C::kStages;
-                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                const int s = i % L::kStages;
+                const uint32_t ph = (uint32_t)(i / L::kStages) & 1u;
                 const int b = i & 1;
                 const uint32_t tph = (uint32_t)(i >> 1) & 1u;
                 if (!mbar_wait(&ct.tempty[b], tph ^ 1u, abort_flag)) break;
@@ -469,8 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; ok && i < ntiles; ++i) {
             if constexpr (F32) {
-                const int s = i % C::kStages;
-                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+                const int s = i % L::kStages;
+                const uint32_t ph = (uint32_t)(i / L::kStages) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(&ct.full[s], ph, abort_flag))) break;
                 split_tf32(sA + s * L::kAStage, sAlo + s * L::kAStage, L::kAStage, et, kEpi);
                 fence_proxy_async();
@@ -504,7 +825,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int j = (c_begin + cc) * (16 / H) + jj;
                         if (j < qv) {
                             const float sc = head_sum<H>(&ct.w[j * H], &v[cc][jj * H]);
-                            if (blk < ct.nb[j]) p.scores[(size_t)(q0 + j) * p.stride + blk] = sc;
+                            if (FUSED) sbuf[j * p.sb_stride + i * kBM + row] = sc;
+                            if ((!FUSED || p.scores) && blk < ct.nb[j])
+                                p.scores[(size_t)(q0 + j) * p.stride + blk] = sc;
                         }
                     }
                 }
@@ -520,7 +843,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
     }
+    }  // ntiles > 0
     if (tid == 0 && ct.abort && p.flags) atomicOr(p.flags, QSA_FLAG_WAIT_TIMEOUT);
+    if constexpr (FUSED) fused_select(p, ct, sbuf, hist, q0, qv, t_begin, max(ntiles, 0));
 }
 
 // ---------------------------------------------------------------- host side
@@ -590,30 +915,31 @@ qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint64_t rows, u
     return QSA_OK;
 }
 
-template <bool F32, int H>
+template <bool F32, int H, bool FUSED>
 qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
                         cudaStream_t s) {
-    constexpr int bytes = smem_bytes<F32>();
+    constexpr int bytes = smem_bytes<F32, FUSED>();
     static_assert(bytes <= 227 * 1024, "scorer shared memory");
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(scorer_tc_kernel<F32, H>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        attr_err = cudaFuncSetAttribute(scorer_tc_kernel<F32, H, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        bytes);
     });
     if (attr_err != cudaSuccess) return check_cuda(attr_err, "cudaFuncSetAttribute(scorer)");
-    scorer_tc_kernel<F32, H><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
-    return check_cuda(cudaGetLastError(), "scorer_tc_kernel launch");
+    scorer_tc_kernel<F32, H, FUSED><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
+    return check_cuda(cudaGetLastError(), FUSED ? "fused scorer+select launch" : "scorer_tc_kernel launch");
 }
 
-template <bool F32>
+template <bool F32, bool FUSED>
 qsa_status launch_heads(int H, const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
                         cudaStream_t s) {
     switch (H) {
-    case 1: return launch_typed<F32, 1>(mk, mq, kp, grid, s);
-    case 2: return launch_typed<F32, 2>(mk, mq, kp, grid, s);
-    case 4: return launch_typed<F32, 4>(mk, mq, kp, grid, s);
-    case 8: return launch_typed<F32, 8>(mk, mq, kp, grid, s);
-    case 16: return launch_typed<F32, 16>(mk, mq, kp, grid, s);
+    case 1: return launch_typed<F32, 1, FUSED>(mk, mq, kp, grid, s);
+    case 2: return launch_typed<F32, 2, FUSED>(mk, mq, kp, grid, s);
+    case 4: return launch_typed<F32, 4, FUSED>(mk, mq, kp, grid, s);
+    case 8: return launch_typed<F32, 8, FUSED>(mk, mq, kp, grid, s);
+    case 16: return launch_typed<F32, 16, FUSED>(mk, mq, kp, grid, s);
     default: return fail(QSA_ERR_INVALID_ARG, "n_heads %d", H);
     }
 }
@@ -624,15 +950,37 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     const bool f32 = a.dt == QSA_F32;
     const int H = a.n_heads;
     const int max_bn = f32 ? Cfg<true>::kMaxBN : Cfg<false>::kMaxBN;
-    const int qg = std::min(a.nq, std::max(1, max_bn / H));
-    const int bn = (qg * H + 15) / 16 * 16;
-    const int groups = (a.nq + qg - 1) / qg;
     const int tiles = (a.bound + kBM - 1) / kBM;
-    if (tiles == 0) return QSA_OK;   // no block can be valid
+    if (tiles == 0 && !a.fused) return QSA_OK;   // no block can be valid
     const int sms = num_sms();
-    int cpg = std::max(1, std::min(tiles, sms / groups));
-    const int tpc = (tiles + cpg - 1) / cpg;
-    cpg = (tiles + tpc - 1) / tpc;
+    const int t1 = std::max(tiles, 1);
+    // queries per group: as many as fill the MMA's N side; the fused kernel keeps at
+    // most 16 on chip (one epilogue warp each) and fewer when their scores or the
+    // merge candidates would not fit
+    int qg = std::min(a.nq, std::max(1, a.fused ? std::min(max_bn / H, kEpi / 32) : max_bn / H));
+    int groups = 0, cpg = 0, tpc = 0;
+    for (;; qg = (qg + 1) / 2) {
+        groups = (a.nq + qg - 1) / qg;
+        cpg = std::max(1, std::min(t1, sms / groups));
+        tpc = (t1 + cpg - 1) / cpg;
+        if (!a.fused) break;
+        const int sbuf = f32 ? sbuf_bytes<true, true>() : sbuf_bytes<false, true>();
+        const int tpc_max = sbuf / (qg * kBM * 4);
+        bool fits = tpc_max >= 1;
+        if (fits) {
+            tpc = std::min(tpc, tpc_max);
+            cpg = (t1 + tpc - 1) / tpc;
+            const long kc = std::min(a.k, tpc * kBM);   // candidates of a full chunk
+            fits = (long)qg * cpg * kc * 8 <= sbuf && cpg <= a.maxch;
+        }
+        if (fits) break;
+        if (qg == 1)
+            return fail(QSA_ERR_UNSUPPORTED,
+                        "fused select: the per-CTA scores or the %d x k = %d merge candidates do not fit on chip; "
+                        "use the chained form", cpg, a.k);
+    }
+    cpg = (t1 + tpc - 1) / tpc;
+    const int bn = (qg * H + 15) / 16 * 16;
     int tmem_cols = 32;
     while (tmem_cols < 2 * bn) tmem_cols *= 2;
 
@@ -655,8 +1003,16 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     kp.tiles_per_cta = tpc;
     kp.tiles_total = tiles;
     kp.tmem_cols = tmem_cols;
+    kp.ids = a.ids;
+    kp.k = a.k;
+    kp.tickets = a.tickets;
+    kp.cand = a.cand;
+    kp.maxch = a.maxch;
+    kp.sb_stride = tpc * kBM;
     const dim3 grid(cpg, groups);
-    return f32 ? launch_heads<true>(H, mk, mq, kp, grid, s) : launch_heads<false>(H, mk, mq, kp, grid, s);
+    if (a.fused)
+        return f32 ? launch_heads<true, true>(H, mk, mq, kp, grid, s) : launch_heads<false, true>(H, mk, mq, kp, grid, s);
+    return f32 ? launch_heads<true, false>(H, mk, mq, kp, grid, s) : launch_heads<false, false>(H, mk, mq, kp, grid, s);
 }
 
 }  // namespace qsa
