@@ -88,7 +88,7 @@ struct ScorerArgs {
     int32_t *ids;
     int k;
     uint32_t *tickets;
-    uint64_t *cand;   // [nq][maxch][k] packed candidates; spans the ckeys and cids regions
+    uint64_t *cand;   // nq * maxch * k packed candidates; spans the ckeys and cids regions
     int maxch;
 };
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);

@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "qsa_device.cuh"
+#include "warp_topk.cuh"
 #include "qsa_internal.h"
 
 namespace qsa {
@@ -108,7 +109,7 @@ struct KParams {
     int32_t *ids;
     int k;
     uint32_t *tickets;
-    uint64_t *cand;    // [nq][maxch][k] packed candidates
+    uint64_t *cand;    // packed candidates; a query group uses nq_group * maxch * k entries from q0 * maxch * k
     int maxch;
     int sb_stride;     // scores per query in the on-chip buffer (tiles_per_cta * 128)
 };
@@ -314,158 +315,9 @@ __device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes,
 
 // ---------------------------------------------------------------- fused select
 
-// Stage A of one query on one CTA, fast form (k <= 32): the exact top-k of the
-// CTA's n > k scores of the query (row[0..n), block ids lo + i), written to
-// dst[0..k) as packed candidates in descending order.  Each lane keeps the two
-// largest keys of its share, the k-th largest of those 64 bounds the answer from
-// below, the keys at or above it (about k + 4 on continuous scores) are gathered
-// into buf at offsets from one warp scan of the lanes' counts, and their exact
-// ranks pick the top k.  Rows of up to 32 * 4 * NV scores are held in registers
-// (one read of shared memory); longer rows are read three times.  Returns false,
-// having written nothing, when more than 64 keys reach the bound (heavy ties).
-template <int NV>
-__device__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
-    const int lane = threadIdx.x & 31;
-    const float4 *r4 = reinterpret_cast<const float4 *>(row);   // rows start on 512-byte boundaries
-    uint32_t key[NV][4];
-#pragma unroll
-    for (int t = 0; t < NV; ++t) {
-        const int v = lane + 32 * t;
-        const float4 f = 4 * v < n ? r4[v] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float e[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) key[t][c] = 4 * v + c < n ? score_key(e[c]) : 0u;
-    }
-    uint32_t a1[4] = {0u, 0u, 0u, 0u}, a2[4] = {0u, 0u, 0u, 0u};   // one top-2 per component
-#pragma unroll
-    for (int t = 0; t < NV; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            a2[c] = max(a2[c], min(a1[c], key[t][c]));
-            a1[c] = max(a1[c], key[t][c]);
-        }
-    uint32_t m1 = a1[0], m2 = a2[0];
-#pragma unroll
-    for (int c = 1; c < 4; ++c) {   // top-2 of two top-2 pairs
-        m2 = max(min(m1, a1[c]), max(m2, a2[c]));
-        m1 = max(m1, a1[c]);
-    }
-    // absent entries have key 0; a zero bound keeps them, which the count below excludes
-    const uint32_t lb = warp_bound_from_top2(m1, m2, k);
-    int nk = 0;
-#pragma unroll
-    for (int t = 0; t < NV; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) nk += 4 * (lane + 32 * t) + c < n && key[t][c] >= lb;
-    const int incl = warp_incl_scan(nk);
-    const int m = __shfl_sync(kFull, incl, 31);
-    if (m > 64) return false;
-    int pos = incl - nk;
-#pragma unroll
-    for (int t = 0; t < NV; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int i = 4 * (lane + 32 * t) + c;
-            if (i < n && key[t][c] >= lb) buf[pos++] = pack_cand(key[t][c], lo + i);
-        }
-    __syncwarp();
-    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
-    return true;
-}
-
-__device__ bool stage_a_smem(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
-    const int lane = threadIdx.x & 31;
-    const float4 *r4 = reinterpret_cast<const float4 *>(row);
-    const int n4 = (n + 3) >> 2;
-    uint32_t a1[4] = {0u, 0u, 0u, 0u}, a2[4] = {0u, 0u, 0u, 0u};
-#pragma unroll 2
-    for (int v = lane; v < n4; v += 32) {
-        const float4 f = r4[v];
-        const float e[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t key = 4 * v + c < n ? score_key(e[c]) : 0u;
-            a2[c] = max(a2[c], min(a1[c], key));
-            a1[c] = max(a1[c], key);
-        }
-    }
-    uint32_t m1 = a1[0], m2 = a2[0];
-#pragma unroll
-    for (int c = 1; c < 4; ++c) {
-        m2 = max(min(m1, a1[c]), max(m2, a2[c]));
-        m1 = max(m1, a1[c]);
-    }
-    const uint32_t lb = warp_bound_from_top2(m1, m2, k);
-    int nk = 0;
-#pragma unroll 2
-    for (int v = lane; v < n4; v += 32) {
-        const float4 f = r4[v];
-        const float e[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) nk += 4 * v + c < n && score_key(e[c]) >= lb;
-    }
-    const int incl = warp_incl_scan(nk);
-    const int m = __shfl_sync(kFull, incl, 31);
-    if (m > 64) return false;
-    int pos = incl - nk;
-    for (int v = lane; v < n4; v += 32) {
-        const float4 f = r4[v];
-        const float e[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t key = score_key(e[c]);
-            if (4 * v + c < n && key >= lb) buf[pos++] = pack_cand(key, lo + 4 * v + c);
-        }
-    }
-    __syncwarp();
-    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
-    return true;
-}
-
-// Stage B of one query, fast form (k <= 32).  list holds the query's chunks, chunk
-// c at list[c * kc], its cnt_c = min(kc, max(0, n - c * S)) candidates in
-// descending order.  The keys of 64 sampled heads (rank e / nch of chunk e % nch,
-// e < 64) bound the k-th largest key from below; the candidates at or above it are
-// a prefix of each chunk, gathered into buf and ranked exactly.  The selected ids
-// go to out[0..k) ascending.  Returns false, having written nothing, when more
-// than 64 candidates reach the bound.
-__device__ bool stage_b_fast(const uint64_t *list, int nch, int kc, int S, int n, int k, uint64_t *buf, int32_t *sid,
-                             int32_t *out) {
-    const int lane = threadIdx.x & 31;
-    uint32_t x[2];
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        const int e = 2 * lane + s, c = e % nch, rr = e / nch;
-        x[s] = rr < min(kc, n - c * S) ? cand_key(list[c * kc + rr]) : 0u;
-    }
-    const uint32_t lb = warp_bound_from_top2(x[0], x[1], k);
-    if (lb == 0u) return false;   // fewer than k heads: no bound
-    int m = 0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-        const int c = c0 + lane;
-        int p = 0;
-        if (c < nch) {
-            const int cc = min(kc, n - c * S);
-            while (p < cc && cand_key(list[c * kc + p]) >= lb) ++p;
-        }
-        const int incl = warp_incl_scan(p);
-        const int off = m + incl - p;
-        for (int i = 0; i < p && off + i < 64; ++i) buf[off + i] = list[c * kc + i];
-        m += __shfl_sync(kFull, incl, 31);
-    }
-    __syncwarp();
-    if (m > 64) return false;
-    warp_rank_top(buf, m, k, [&](int r, uint64_t c) { sid[r] = cand_id(c); });
-    int32_t id = lane < k ? sid[lane] : 0x7fffffff;
-    warp_sort32_asc(id);
-    if (lane < k) out[lane] = id;
-    __syncwarp();
-    return true;
-}
-
 // The selection tail of the fused kernel.  Stage A: each epilogue warp takes the
 // queries j = warp, warp + 16, ... of the group and writes the top min(n_loc, k)
-// of this CTA's blocks of the query to cand[q][chunk] (descending for k <= 32,
+// of this CTA's blocks of the query to the workspace (descending for k <= 32,
 // else in block order).  The CTA then takes a ticket; the last CTA of the group
 // runs stage B: it loads every chunk's candidates of every query into shared
 // memory (a chunk c holds min(k, max(0, n - c * S)) of them, S = blocks per CTA,
@@ -490,6 +342,12 @@ __device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbu
     uint64_t *buf = reinterpret_cast<uint64_t *>(h);
     int32_t *sid = reinterpret_cast<int32_t *>(h + 160);
     const bool fast = k <= 32;
+    const int S = sb_stride;             // blocks per CTA
+    const int kc = min(k, S);            // candidates of a full chunk
+    const int per = nch * kc;            // candidates of a query
+    // the group's candidates are one contiguous run, query j's list at j * per and
+    // its chunk c at j * per + c * kc: the layout stage B keeps in shared memory
+    uint64_t *const __restrict__ gcand = cand + (size_t)q0 * maxch * k;
     if (ew >= 0) {
         for (int i = lane; i < 256; i += 32) h[i] = 0u;
         __syncwarp();
@@ -499,7 +357,7 @@ __device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbu
             const int n = ct.nb[j];
             if (n <= k) continue;   // stage B emits 0..n-1
             const int nloc = max(0, min(ntiles * kBM, n - lo));
-            uint64_t *dst = cand + ((size_t)q * maxch + c) * k;
+            uint64_t *dst = gcand + (size_t)j * per + (size_t)c * kc;
             const float *row = sbuf + (size_t)j * sb_stride;   // this CTA's blocks of query j
             if (nloc <= k) {
                 for (int i = lane; i < nloc; i += 32) dst[i] = pack_cand(score_key(row[i]), lo + i);
@@ -534,45 +392,28 @@ __device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbu
             }
         }
     }
-    __threadfence();
     __syncthreads();
-    if (tid == 0) ct.last = atomicAdd(&tickets[g], 1u) == (unsigned)nch - 1u;
+    if (tid == 0) {   // the barrier orders the CTA's candidate writes before this fence
+        __threadfence();
+        ct.last = atomicAdd(&tickets[g], 1u) == (unsigned)nch - 1u;
+    }
     __syncthreads();
     if (!ct.last) return;
     if (tid == 0) __threadfence();
     __syncthreads();
-    // every candidate of the group into shared memory: query j's list at lists[j * per],
-    // a warp per (query, chunk) row, a lane per candidate, kR rows in flight
-    const int S = sb_stride;             // blocks per CTA
-    const int kc = min(k, S);            // candidates of a full chunk
-    const int per = nch * kc;
+    // every candidate of the group into shared memory, one flat copy (entries a
+    // chunk did not fill are copied too and never read)
     uint64_t *lists = reinterpret_cast<uint64_t *>(sbuf);
     {
-        constexpr int kWarps = kThreads / 32, kR = 8;
-        const int rows = qv * nch;
-        for (int i0 = 0; i0 < kc; i0 += 32) {
-            const int i = i0 + lane;
-            for (int r0 = warp; r0 < rows; r0 += kWarps * kR) {
-                uint64_t v[kR];
-                int at[kR];
+        constexpr int kU = 8;   // loads in flight per thread
+        const int total = qv * per;
+        for (int e0 = tid; e0 < total; e0 += kThreads * kU) {
+            uint64_t v[kU];
 #pragma unroll
-                for (int u = 0; u < kR; ++u) {
-                    const int r = r0 + u * kWarps;
-                    at[u] = -1;
-                    v[u] = 0ull;
-                    if (r < rows) {
-                        const int j = r / nch, cc = r - j * nch;
-                        const int n = ct.nb[j];
-                        if (n > k && i < min(kc, n - cc * S)) {
-                            v[u] = __ldcg(cand + ((size_t)(q0 + j) * maxch + cc) * k + i);
-                            at[u] = j * per + cc * kc + i;
-                        }
-                    }
-                }
+            for (int u = 0; u < kU; ++u) v[u] = __ldcg(gcand + min(e0 + u * kThreads, total - 1));
 #pragma unroll
-                for (int u = 0; u < kR; ++u)
-                    if (at[u] >= 0) lists[at[u]] = v[u];
-            }
+            for (int u = 0; u < kU; ++u)
+                if (e0 + u * kThreads < total) lists[e0 + u * kThreads] = v[u];
         }
     }
     __syncthreads();
