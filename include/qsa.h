@@ -72,7 +72,9 @@ typedef enum {
     QSA_PATH_SPLIT = 1,    /* multi-CTA chunk split + last-CTA merge (decode windows) */
     QSA_PATH_SAMPLE = 2,   /* one read against a sampled lower bound (+ radix fallback) */
     QSA_PATH_REGISTER = 3, /* whole row in registers, one CTA per query */
-    QSA_PATH_RADIX = 4     /* multi-pass radix select over global memory, any size */
+    QSA_PATH_RADIX = 4,    /* multi-pass radix select over global memory, any size */
+    QSA_PATH_WARP = 5      /* k <= 32: one warp per 1,024-block chunk bounds, filters and ranks its
+                              chunk in registers, one warp merges (rows of up to 8,192 blocks) */
 } qsa_path;
 
 typedef void *qsa_stream; /* a cudaStream_t */

@@ -69,8 +69,15 @@ static int effective_bound(int max_blocks, int active_blocks) {
 // register path reads the row once too and has no sampling step.
 static constexpr int kSampleMinBlocks = 2048;
 
+// Rows of up to 8,192 blocks at k <= 32 (every workload of the pages) take the warp
+// path: one HBM read per row and no block-wide barrier in the selection; on GB300 it
+// beats the split (decode), sampled (prompt) and register paths at every such size.
+static constexpr int kWarpPathMaxK = 32;
+static constexpr int kWarpPathMaxBlocks = 8192;
+
 static qsa_path auto_path(int nq, int max_blocks, int active_blocks, int k) {
     const int bound = effective_bound(max_blocks, active_blocks);
+    if (k <= kWarpPathMaxK && bound <= kWarpPathMaxBlocks) return QSA_PATH_WARP;
     const WsLayout L = ws_layout(nq, max_blocks, k);
     if (active_blocks < 0 && nq <= 16 && bound > k && split_geometry(bound, nq, k, L.maxch).chunk_len > 0)
         return QSA_PATH_SPLIT;
@@ -165,6 +172,8 @@ static qsa_status run_topk(const float *scores, int64_t stride, const int32_t *n
         return launch_topk_register(a, s);
     case QSA_PATH_RADIX:
         return launch_topk_radix(a, false, s);
+    case QSA_PATH_WARP:
+        return launch_topk_warp(a, s);
     default:
         return fail(QSA_ERR_INVALID_ARG, "bad path %d", (int)path);
     }

@@ -25,6 +25,7 @@
 
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
+#include "warp_topk.cuh"
 
 namespace qsa {
 
@@ -417,6 +418,87 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
     if (threadIdx.x == 0) a.tickets[q] = 0u;
 }
 
+// ---------------------------------------------------------------------------- warp path
+//
+// k <= 32, rows of up to NW * 1,024 blocks, one CTA of NW warps per query.  Warp
+// w takes blocks [1024 w, 1024 (w + 1)) of the row into registers (one read of
+// HBM), bounds the chunk's k-th largest key from below with the k-th largest of
+// the lanes' top-2 keys, keeps the entries at or above it (a few more than k on
+// continuous scores) and ranks them exactly: its chunk's top k, descending, in
+// shared memory.  Warp 0 then merges the chunks' lists the same way.  A query's
+// selection restricted to a chunk is a prefix of that chunk's order, so every
+// selected block is among its chunk's k (the split of Strata PR #3987, section
+// "Approach").  Heavy ties (more than 64 entries at the bound) take the radix
+// warp select instead.
+
+constexpr int kWarpChunk = 1024;
+
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
+    __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
+    __shared__ __align__(16) uint64_t lists[NW * 32];      // per chunk: its top k, descending
+    const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
+    const int k = a.k;
+    int32_t *out = a.ids + (size_t)q * k;
+    if (n <= k) {
+        emit_all(n, k, out);
+        return;
+    }
+    const float *row = a.scores + (size_t)q * a.stride;
+    uint32_t *h = scratch[warp];
+    uint64_t *buf = reinterpret_cast<uint64_t *>(h);
+    for (int i = lane; i < 256; i += 32) h[i] = 0u;
+    __syncwarp();
+    const int lo = warp * kWarpChunk;
+    const int len = min(kWarpChunk, n - lo);
+    uint64_t *dst = lists + warp * k;
+    if (len > k) {
+        const float *r = row + lo;
+        const float4 *r4 = reinterpret_cast<const float4 *>(r);
+        const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
+        const bool ok = warp_top_regs<kWarpChunk / 128>(
+            [&](int v) {
+                if (vec && 4 * v + 3 < len) return __ldcs(r4 + v);
+                float e[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) e[c] = 4 * v + c < len ? __ldcs(r + 4 * v + c) : 0.0f;
+                return make_float4(e[0], e[1], e[2], e[3]);
+            },
+            len, k, lo, buf, dst);
+        if (!ok) {
+            for (int i = lane; i < 256; i += 32) h[i] = 0u;
+            __syncwarp();
+            warp_select([&](int i) { return score_key(__ldg(r + i)); }, len, k, h,
+                        [&](int pos, int i) { dst[pos] = pack_cand(score_key(__ldg(r + i)), lo + i); });
+            __syncwarp();
+            uint64_t v = lane < k ? ~dst[lane] : ~0ull;   // descending, like the other chunks
+            __syncwarp();
+            warp_sort32_asc(v);
+            if (lane < k) dst[lane] = ~v;
+        }
+    } else if (len > 0) {
+        uint64_t v = lane < len ? ~pack_cand(score_key(__ldcs(row + lo + lane)), lo + lane) : ~0ull;
+        warp_sort32_asc(v);
+        if (lane < len) dst[lane] = ~v;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int nch = (n + kWarpChunk - 1) / kWarpChunk;
+    const int full = n / kWarpChunk;
+    const int L = full * k + min(k, n - full * kWarpChunk);
+    int32_t *sid = reinterpret_cast<int32_t *>(h + 160);
+    if (L > k && stage_b_fast(lists, nch, k, kWarpChunk, n, k, buf, sid, out)) return;
+    for (int i = lane; i < 256; i += 32) h[i] = 0u;
+    __syncwarp();
+    warp_select([&](int i) { return lists[i]; }, L, k, h, [&](int pos, int i) { out[pos] = cand_id(lists[i]); });
+    __syncwarp();
+    int32_t id = lane < min(L, k) ? out[lane] : 0x7fffffff;
+    __syncwarp();
+    warp_sort32_asc(id);
+    if (lane < k) out[lane] = lane < L ? id : -1;
+}
+
 // ---------------------------------------------------------------------------- launchers
 
 template <bool SAMPLE>
@@ -439,6 +521,24 @@ static qsa_status launch_row(const TopkArgs &a, cudaStream_t s) {
 qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s) { return launch_row<false>(a, s); }
 
 qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) { return launch_row<true>(a, s); }
+
+qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s) {
+    if (a.k > 32)
+        return fail(QSA_ERR_UNSUPPORTED, "warp path takes k <= 32 (got %d)", a.k);
+    if (a.bound <= kWarpChunk) {
+        topk_warp_kernel<1><<<a.nq, 32, 0, s>>>(a);
+    } else if (a.bound <= 2 * kWarpChunk) {
+        topk_warp_kernel<2><<<a.nq, 64, 0, s>>>(a);
+    } else if (a.bound <= 4 * kWarpChunk) {
+        topk_warp_kernel<4><<<a.nq, 128, 0, s>>>(a);
+    } else if (a.bound <= 8 * kWarpChunk) {
+        topk_warp_kernel<8><<<a.nq, 256, 0, s>>>(a);
+    } else {
+        return fail(QSA_ERR_UNSUPPORTED, "warp path holds at most %d blocks per row (bound %d)", 8 * kWarpChunk,
+                    a.bound);
+    }
+    return check_cuda(cudaGetLastError(), "topk_warp_kernel launch");
+}
 
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s) {
     topk_radix_kernel<512><<<a.nq, 512, 0, s>>>(a, flagged_only ? 1 : 0);

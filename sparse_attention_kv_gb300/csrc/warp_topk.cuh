@@ -24,16 +24,23 @@ namespace qsa {
 // ranks pick the top k.  Rows of up to 32 * 4 * NV scores are held in registers
 // (one read of shared memory); longer rows are read three times.  Returns false,
 // having written nothing, when more than 64 keys reach the bound (heavy ties).
-template <int NV>
-__device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
+// load4(v) returns row entries 4v .. 4v + 3 (called for 4v < n; entries at or past
+// n may hold anything).
+template <int NV, typename Load4>
+__device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const int lane = threadIdx.x & 31;
-    const float4 *r4 = reinterpret_cast<const float4 *>(row);   // rows start on 512-byte boundaries
+    // every load in flight before the first use
+    float4 f[NV];
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        const int v = lane + 32 * t;
+        f[t] = 4 * v < n ? load4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     uint32_t key[NV][4];
 #pragma unroll
     for (int t = 0; t < NV; ++t) {
         const int v = lane + 32 * t;
-        const float4 f = 4 * v < n ? r4[v] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float e[4] = {f.x, f.y, f.z, f.w};
+        const float e[4] = {f[t].x, f[t].y, f[t].z, f[t].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) key[t][c] = 4 * v + c < n ? score_key(e[c]) : 0u;
     }
@@ -72,6 +79,14 @@ __device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int
     __syncwarp();
     warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
     return true;
+}
+
+// The register form on a shared-memory row whose storage extends to a multiple of
+// four entries past n (the fused kernel's rows start on 512-byte boundaries).
+template <int NV>
+__device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+    return warp_top_regs<NV>([&](int v) { return r4[v]; }, n, k, lo, buf, dst);
 }
 
 __device__ __forceinline__ bool stage_a_smem(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {

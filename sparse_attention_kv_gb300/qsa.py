@@ -21,9 +21,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 # qsa_dtype
 F32, BF16 = 0, 1
 # qsa_path
-PATH_AUTO, PATH_SPLIT, PATH_SAMPLE, PATH_REGISTER, PATH_RADIX = range(5)
+PATH_AUTO, PATH_SPLIT, PATH_SAMPLE, PATH_REGISTER, PATH_RADIX, PATH_WARP = range(6)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SPLIT: "split", PATH_SAMPLE: "sample",
-              PATH_REGISTER: "register", PATH_RADIX: "radix"}
+              PATH_REGISTER: "register", PATH_RADIX: "radix", PATH_WARP: "warp"}
 # flags word bits
 FLAG_NBLOCKS_CLAMPED, FLAG_WAIT_TIMEOUT, FLAG_INTERNAL, FLAG_SAMPLE_FALLBACK = 0x1, 0x2, 0x4, 0x8
 ERROR_FLAGS = FLAG_NBLOCKS_CLAMPED | FLAG_WAIT_TIMEOUT | FLAG_INTERNAL

@@ -48,16 +48,22 @@ def test_workspace_sizes(lib):
 
 
 def test_auto_path_rules(lib):
-    # decode window (no active count, few queries): split
-    assert lib.qsa_auto_path(3, 4096, -1, 32) == qsa.PATH_SPLIT
-    assert lib.qsa_auto_path(16, 4096, -1, 32) == qsa.PATH_SPLIT
+    # k <= 32 and rows of up to 8,192 blocks: the warp path, decode and prompt alike
+    for nq, mb, act in ((3, 4096, -1), (16, 4096, -1), (256, 8192, 8125), (256, 2048, 2048), (256, 8192, 1000),
+                        (1, 8192, -1)):
+        assert lib.qsa_auto_path(nq, mb, act, 32) == qsa.PATH_WARP
+        assert lib.qsa_auto_path(nq, mb, act, 1) == qsa.PATH_WARP
+    # larger k: decode windows (no active count, few queries) split
+    assert lib.qsa_auto_path(3, 4096, -1, 64) == qsa.PATH_SPLIT
+    assert lib.qsa_auto_path(16, 4096, -1, 64) == qsa.PATH_SPLIT
     # prompt calls: sampled filter past the threshold, register below it
-    assert lib.qsa_auto_path(256, 8192, 8125, 32) == qsa.PATH_SAMPLE
-    assert lib.qsa_auto_path(256, 2048, 2048, 32) == qsa.PATH_SAMPLE
-    assert lib.qsa_auto_path(256, 8192, 1000, 32) == qsa.PATH_REGISTER
+    assert lib.qsa_auto_path(256, 8192, 8125, 64) == qsa.PATH_SAMPLE
+    assert lib.qsa_auto_path(256, 2048, 2048, 64) == qsa.PATH_SAMPLE
+    assert lib.qsa_auto_path(256, 8192, 1000, 64) == qsa.PATH_REGISTER
     # beyond the on-chip reach: radix
     assert lib.qsa_auto_path(256, 100000, 100000, 32) == qsa.PATH_RADIX
     assert lib.qsa_auto_path(64, 100000, -1, 32) == qsa.PATH_RADIX
+    assert lib.qsa_auto_path(256, 8193, 8193, 32) == qsa.PATH_RADIX
 
 
 FAKE = 0x10000   # never dereferenced: each call below fails validation first

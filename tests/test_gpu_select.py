@@ -86,7 +86,7 @@ def test_stress_end_to_end(kind):
         np.testing.assert_array_equal(ids, np.tile(np.arange(case.k, dtype=np.int32), (case.nq, 1)))
 
 
-@pytest.mark.parametrize("path", [qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_SPLIT])
+@pytest.mark.parametrize("path", [qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_SPLIT, qsa.PATH_WARP])
 def test_every_path_end_to_end_on_decode_and_prompt(path):
     for case in (inputs.decode_case(1), inputs.prompt_case()):
         try:

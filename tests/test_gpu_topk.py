@@ -17,7 +17,7 @@ if not torch.cuda.is_available():
 
 from sparse_attention_kv_gb300 import qsa  # noqa: E402
 
-PATHS = [qsa.PATH_AUTO, qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_SPLIT]
+PATHS = [qsa.PATH_AUTO, qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_SPLIT, qsa.PATH_WARP]
 
 
 def run_topk(scores_np, n_blocks_np, k, path, active=-1, max_blocks=None, stride=None):
@@ -36,7 +36,9 @@ def run_topk(scores_np, n_blocks_np, k, path, active=-1, max_blocks=None, stride
 
 def _supported(path, C, nq, k, active):
     bound = C if active < 0 else min(active, C)
-    if path in (qsa.PATH_REGISTER, qsa.PATH_SAMPLE) and bound > 8192:
+    if path in (qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_WARP) and bound > 8192:
+        return False
+    if path == qsa.PATH_WARP and k > 32:
         return False
     return True
 
@@ -119,7 +121,7 @@ def test_topk_k_range(path, k):
     np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
 
 
-@pytest.mark.parametrize("path", [qsa.PATH_AUTO, qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE])
+@pytest.mark.parametrize("path", [qsa.PATH_AUTO, qsa.PATH_RADIX, qsa.PATH_REGISTER, qsa.PATH_SAMPLE, qsa.PATH_WARP])
 def test_topk_unaligned_stride_uses_scalar_loads(path):
     nq, C, k = 6, 3001, 32
     sc = inputs.normal_scores(6400, nq, C)
@@ -184,3 +186,29 @@ def test_sample_few_candidates_falls_back(k):
     ids, flags, ws = run_topk(sc, nb, k, qsa.PATH_SAMPLE, active=8192)
     np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
     assert flags & qsa.ERROR_FLAGS == 0
+
+
+@pytest.mark.parametrize("n", [33, 64, 65, 1023, 1024, 1025, 2047, 2048, 4097, 8191, 8192])
+@pytest.mark.parametrize("kind", ["normal", "levels", "equal"])
+def test_warp_path_chunk_boundaries(n, kind):
+    """Rows that end inside, at and just past a warp's 1,024-block chunk, with continuous,
+    quantised and all-equal scores (the last two take the radix fallbacks)."""
+    nq, C, k = 4, 8192, 32
+    seed = 6900 + n
+    sc = (inputs.normal_scores(seed, nq, C) if kind == "normal" else
+          inputs.level_scores(seed, nq, C) if kind == "levels" else np.full((nq, C), 0.5, dtype=np.float32))
+    nb = np.array([n, max(n - 1, 0), min(n + 1, C), n], dtype=np.int32)
+    ids, flags, _ = run_topk(sc, nb, k, qsa.PATH_WARP, active=C)
+    np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
+    assert flags & qsa.ERROR_FLAGS == 0
+
+
+def test_warp_path_rejects_large_k_and_long_rows():
+    sc = inputs.normal_scores(6950, 2, 9000)
+    nb = np.array([9000, 100], dtype=np.int32)
+    with pytest.raises(qsa.QSAError) as e:
+        run_topk(sc, nb, 32, qsa.PATH_WARP, active=9000)
+    assert e.value.status == qsa.ERR_UNSUPPORTED
+    with pytest.raises(qsa.QSAError) as e:
+        run_topk(sc[:, :4096], np.array([4096, 100], dtype=np.int32), 33, qsa.PATH_WARP, active=4096)
+    assert e.value.status == qsa.ERR_UNSUPPORTED
