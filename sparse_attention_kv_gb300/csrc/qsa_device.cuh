@@ -22,6 +22,15 @@ __device__ __forceinline__ uint32_t score_key(float x) {
     return u ^ ((u & 0x80000000u) ? 0xffffffffu : 0x80000000u);
 }
 
+// Programmatic dependent launch.  wait_prior_grid() blocks until the grid launched
+// before this one on the stream has completed and its memory writes are visible; it
+// returns at once when this grid was launched without the programmatic attribute.
+// allow_dependent_launch() lets a grid launched after this one with that attribute
+// start its CTAs (which then wait in wait_prior_grid) once every CTA of this grid
+// has executed it or exited.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ int warp_incl_scan(int v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll

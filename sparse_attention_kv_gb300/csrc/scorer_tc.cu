@@ -679,6 +679,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
+    // A dependent grid (the top-k of a chained select) starts once every CTA of this
+    // grid has passed this point or exited, so no scorer CTA can still be waiting for
+    // the SM a waiting top-k CTA takes.
+    allow_dependent_launch();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

@@ -126,6 +126,7 @@ struct __align__(16) RowSmem {
 
 template <int R, bool SAMPLE>
 __global__ void __launch_bounds__(kNT, 2) topk_row_kernel(TopkArgs a) {
+    wait_prior_grid();   // the scores may come from the kernel launched just before
     constexpr int KPT = R * 4;
     static_assert(2 * kSampleCap == kRegisterCap, "candidate scores and ids share cand[]");
     __shared__ RowSmem sm;
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_row_kernel(TopkArgs a) {
 
 template <int NT>
 __global__ void __launch_bounds__(NT) topk_radix_kernel(TopkArgs a, int flagged_only) {
+    wait_prior_grid();   // the scores may come from the kernel launched just before
     __shared__ BlockScratch sm;
     const int q = blockIdx.x;
     if (flagged_only && a.qflags[q] == 0u) return;
@@ -326,6 +328,7 @@ struct __align__(16) SplitSmem {
 };
 
 __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chunk_len) {
+    wait_prior_grid();   // the scores may come from the kernel launched just before
     __shared__ SplitSmem sm;
     const int q = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
     const int k = a.k;
@@ -435,6 +438,7 @@ constexpr int kWarpChunk = 1024;
 
 template <int NW>
 __global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
+    wait_prior_grid();   // the scores may come from the kernel launched just before
     __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
     __shared__ __align__(16) uint64_t lists[NW * 32];      // per chunk: its top k, descending
     const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -501,21 +505,35 @@ __global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
 
 // ---------------------------------------------------------------------------- launchers
 
+// Every top-k kernel is launched as a programmatic dependent of the kernel before it
+// on the stream (the scorer, in a chained select): its CTAs may be scheduled while
+// that kernel drains and wait at entry until it has completed.
+template <typename... KArgs, typename... Args>
+static qsa_status launch_dependent(const char *what, void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                                   Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, kern, args...), what);
+}
+
 template <bool SAMPLE>
 static qsa_status launch_row(const TopkArgs &a, cudaStream_t s) {
-    if (a.bound <= 1024) {
-        topk_row_kernel<1, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
-    } else if (a.bound <= 2048) {
-        topk_row_kernel<2, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
-    } else if (a.bound <= 4096) {
-        topk_row_kernel<4, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
-    } else if (a.bound <= kRegisterCap) {
-        topk_row_kernel<8, SAMPLE><<<a.nq, kNT, 0, s>>>(a);
-    } else {
-        return fail(QSA_ERR_UNSUPPORTED, "%s path holds at most %d blocks per row (bound %d)",
-                    SAMPLE ? "sample" : "register", kRegisterCap, a.bound);
-    }
-    return check_cuda(cudaGetLastError(), SAMPLE ? "topk_row_kernel<sample> launch" : "topk_row_kernel launch");
+    const char *what = SAMPLE ? "topk_row_kernel<sample> launch" : "topk_row_kernel launch";
+    const dim3 grid(a.nq), block(kNT);
+    if (a.bound <= 1024) return launch_dependent(what, topk_row_kernel<1, SAMPLE>, grid, block, s, a);
+    if (a.bound <= 2048) return launch_dependent(what, topk_row_kernel<2, SAMPLE>, grid, block, s, a);
+    if (a.bound <= 4096) return launch_dependent(what, topk_row_kernel<4, SAMPLE>, grid, block, s, a);
+    if (a.bound <= kRegisterCap) return launch_dependent(what, topk_row_kernel<8, SAMPLE>, grid, block, s, a);
+    return fail(QSA_ERR_UNSUPPORTED, "%s path holds at most %d blocks per row (bound %d)",
+                SAMPLE ? "sample" : "register", kRegisterCap, a.bound);
 }
 
 qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s) { return launch_row<false>(a, s); }
@@ -525,24 +543,19 @@ qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) { return launch
 qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s) {
     if (a.k > 32)
         return fail(QSA_ERR_UNSUPPORTED, "warp path takes k <= 32 (got %d)", a.k);
-    if (a.bound <= kWarpChunk) {
-        topk_warp_kernel<1><<<a.nq, 32, 0, s>>>(a);
-    } else if (a.bound <= 2 * kWarpChunk) {
-        topk_warp_kernel<2><<<a.nq, 64, 0, s>>>(a);
-    } else if (a.bound <= 4 * kWarpChunk) {
-        topk_warp_kernel<4><<<a.nq, 128, 0, s>>>(a);
-    } else if (a.bound <= 8 * kWarpChunk) {
-        topk_warp_kernel<8><<<a.nq, 256, 0, s>>>(a);
-    } else {
-        return fail(QSA_ERR_UNSUPPORTED, "warp path holds at most %d blocks per row (bound %d)", 8 * kWarpChunk,
-                    a.bound);
-    }
-    return check_cuda(cudaGetLastError(), "topk_warp_kernel launch");
+    const char *what = "topk_warp_kernel launch";
+    const dim3 grid(a.nq);
+    if (a.bound <= kWarpChunk) return launch_dependent(what, topk_warp_kernel<1>, grid, dim3(32), s, a);
+    if (a.bound <= 2 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<2>, grid, dim3(64), s, a);
+    if (a.bound <= 4 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<4>, grid, dim3(128), s, a);
+    if (a.bound <= 8 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<8>, grid, dim3(256), s, a);
+    return fail(QSA_ERR_UNSUPPORTED, "warp path holds at most %d blocks per row (bound %d)", 8 * kWarpChunk,
+                a.bound);
 }
 
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s) {
-    topk_radix_kernel<512><<<a.nq, 512, 0, s>>>(a, flagged_only ? 1 : 0);
-    return check_cuda(cudaGetLastError(), "topk_radix_kernel launch");
+    return launch_dependent("topk_radix_kernel launch", topk_radix_kernel<512>, dim3(a.nq), dim3(512), s, a,
+                            flagged_only ? 1 : 0);
 }
 
 SplitGeom split_geometry(int bound, int nq, int k, int maxch) {
@@ -567,9 +580,8 @@ SplitGeom split_geometry(int bound, int nq, int k, int maxch) {
 qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s) {
     if (g.chunk_len <= 0 || g.chunk_len > kSplitMaxChunk)
         return fail(QSA_ERR_UNSUPPORTED, "split path: no chunk geometry fits (bound %d, k %d)", a.bound, a.k);
-    const dim3 grid(g.nchunks, a.nq);
-    topk_split_kernel<<<grid, kNT, 0, s>>>(a, g.chunk_len);
-    return check_cuda(cudaGetLastError(), "topk_split_kernel launch");
+    return launch_dependent("topk_split_kernel launch", topk_split_kernel, dim3(g.nchunks, a.nq), dim3(kNT), s, a,
+                            g.chunk_len);
 }
 
 }  // namespace qsa
