@@ -83,7 +83,6 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort;
     int maxn;
-    int epi_ok[2];
     int last;
     __align__(16) float w[256];
     int nb[256];
@@ -273,8 +272,6 @@ __device__ __forceinline__ float head_sum(const float *w, const uint32_t *acc) {
     }
 }
 
-// Named barrier 1 over the epilogue warps (barrier 0 is __syncthreads).
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpi) : "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -640,11 +637,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = i & 1;
             const uint32_t tph = (uint32_t)(i >> 1) & 1u;
-            // One thread waits for the accumulator; the other epilogue threads
-            // block on a hardware barrier, which takes no issue slots.
-            if (et == 0) ct.epi_ok[b] = mbar_wait(&ct.tfull[b], tph, abort_flag) ? 1 : 0;
-            epilogue_sync();
-            if (!ct.epi_ok[b]) break;   // uniform across the epilogue
+            // Lane 0 of each warp waits for the accumulator (a suspending try-wait)
+            // and the warp goes on by itself: no epilogue-wide barrier per tile, so a
+            // slow warp delays only its own share.
+            int acc_ok = 0;
+            if (lane == 0) acc_ok = mbar_wait(&ct.tfull[b], tph, abort_flag) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, acc_ok, 0)) break;
             tc_fence_after();
             const int blk = (t_begin + i) * kBM + row;
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * buf_cols);

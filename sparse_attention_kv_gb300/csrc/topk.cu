@@ -428,11 +428,12 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
 // HBM), bounds the chunk's k-th largest key from below with the k-th largest of
 // the lanes' top-2 keys, keeps the entries at or above it (a few more than k on
 // continuous scores) and ranks them exactly: its chunk's top k, descending, in
-// shared memory.  Warp 0 then merges the chunks' lists the same way.  A query's
-// selection restricted to a chunk is a prefix of that chunk's order, so every
-// selected block is among its chunk's k (the split of Strata PR #3987, section
-// "Approach").  Heavy ties (more than 64 entries at the bound) take the radix
-// warp select instead.
+// shared memory.  The chunks' lists are then merged by exact ranks (one thread per
+// candidate, binary searches in the other lists).  A query's selection restricted
+// to a chunk is a prefix of that chunk's order, so every selected block is among
+// its chunk's k (the split of Strata PR #3987, section "Approach").  Heavy ties
+// (more than 64 entries at a chunk's bound) take the radix warp select for that
+// chunk instead.
 
 constexpr int kWarpChunk = 1024;
 
@@ -487,20 +488,37 @@ __global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
         if (lane < len) dst[lane] = ~v;
     }
     __syncthreads();
-    if (warp != 0) return;
+    // Merge: every chunk's list is descending, so a candidate's rank in the whole row
+    // is its index in its own list plus, for every other list, the number of entries
+    // above it (a binary search); packed values are distinct, so the ranks are a
+    // permutation and exactly k candidates rank below k.  One thread per candidate.
+    __shared__ int32_t sel[32];
     const int nch = (n + kWarpChunk - 1) / kWarpChunk;
-    const int full = n / kWarpChunk;
-    const int L = full * k + min(k, n - full * kWarpChunk);
-    int32_t *sid = reinterpret_cast<int32_t *>(h + 160);
-    if (L > k && stage_b_fast(lists, nch, k, kWarpChunk, n, k, buf, sid, out)) return;
-    for (int i = lane; i < 256; i += 32) h[i] = 0u;
-    __syncwarp();
-    warp_select([&](int i) { return lists[i]; }, L, k, h, [&](int pos, int i) { out[pos] = cand_id(lists[i]); });
-    __syncwarp();
-    int32_t id = lane < min(L, k) ? out[lane] : 0x7fffffff;
-    __syncwarp();
-    warp_sort32_asc(id);
-    if (lane < k) out[lane] = lane < L ? id : -1;
+    auto cnt_of = [&](int c) { return c < nch ? min(k, n - c * kWarpChunk) : 0; };
+    if (lane < cnt_of(warp)) {
+        const uint64_t x = lists[warp * k + lane];
+        int rank = lane;
+#pragma unroll
+        for (int b = 0; b < NW; ++b) {
+            if (b == warp) continue;
+            const int cb = cnt_of(b);
+            const uint64_t *lb = lists + b * k;
+            int pos = 0;   // entries of list b above x
+#pragma unroll
+            for (int step = 32; step >= 1; step >>= 1)
+                if (pos + step <= cb && lb[pos + step - 1] > x) pos += step;
+            rank += pos;
+        }
+        if (rank < k) sel[rank] = cand_id(x);
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    if (lane < k) {   // ascending ids: each id's slot is the number of selected ids below it
+        const int32_t id = sel[lane];
+        int below = 0;
+        for (int t = 0; t < k; ++t) below += sel[t] < id;
+        out[below] = id;
+    }
 }
 
 // ---------------------------------------------------------------------------- launchers
