@@ -17,9 +17,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // Order-preserving key of an fp32 score: unsigned order of the keys equals the
 // float order of the scores, -0 and +0 give the same key.  NaN is not ordered.
 __device__ __forceinline__ uint32_t score_key(float x) {
-    uint32_t u = __float_as_uint(x);
-    if (u == 0x80000000u) u = 0u;                      // -0 -> +0
-    return u ^ ((u & 0x80000000u) ? 0xffffffffu : 0x80000000u);
+    const uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));   // -0 + 0 = +0; every other score unchanged
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 // Programmatic dependent launch.  wait_prior_grid() blocks until the grid launched

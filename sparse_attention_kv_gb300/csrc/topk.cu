@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
 constexpr int kWarpChunk = 1024;
 
 template <int NW>
-__global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
     __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
     __shared__ __align__(16) uint64_t lists[NW * 32];      // per chunk: its top k, descending
@@ -462,15 +462,18 @@ __global__ void __launch_bounds__(NW * 32, 3) topk_warp_kernel(TopkArgs a) {
         const float *r = row + lo;
         const float4 *r4 = reinterpret_cast<const float4 *>(r);
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
-        const bool ok = warp_top_regs<kWarpChunk / 128>(
-            [&](int v) {
-                if (vec && 4 * v + 3 < len) return __ldcs(r4 + v);
-                float e[4];
+        const bool ok =
+            vec && len == kWarpChunk
+                ? warp_top_regs<kWarpChunk / 128, true>([&](int v) { return __ldcs(r4 + v); }, len, k, lo, buf, dst)
+                : warp_top_regs<kWarpChunk / 128>(
+                      [&](int v) {
+                          if (vec && 4 * v + 3 < len) return __ldcs(r4 + v);
+                          float e[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) e[c] = 4 * v + c < len ? __ldcs(r + 4 * v + c) : 0.0f;
-                return make_float4(e[0], e[1], e[2], e[3]);
-            },
-            len, k, lo, buf, dst);
+                          for (int c = 0; c < 4; ++c) e[c] = 4 * v + c < len ? __ldcs(r + 4 * v + c) : 0.0f;
+                          return make_float4(e[0], e[1], e[2], e[3]);
+                      },
+                      len, k, lo, buf, dst);
         if (!ok) {
             for (int i = lane; i < 256; i += 32) h[i] = 0u;
             __syncwarp();

@@ -25,8 +25,9 @@ namespace qsa {
 // (one read of shared memory); longer rows are read three times.  Returns false,
 // having written nothing, when more than 64 keys reach the bound (heavy ties).
 // load4(v) returns row entries 4v .. 4v + 3 (called for 4v < n; entries at or past
-// n may hold anything).
-template <int NV, typename Load4>
+// n may hold anything).  FULL: the caller guarantees n == 128 * NV, and no entry is
+// tested against n.
+template <int NV, bool FULL = false, typename Load4>
 __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const int lane = threadIdx.x & 31;
     // every load in flight before the first use
@@ -34,7 +35,7 @@ __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int l
 #pragma unroll
     for (int t = 0; t < NV; ++t) {
         const int v = lane + 32 * t;
-        f[t] = 4 * v < n ? load4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[t] = FULL || 4 * v < n ? load4(v) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     uint32_t key[NV][4];
 #pragma unroll
@@ -42,7 +43,7 @@ __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int l
         const int v = lane + 32 * t;
         const float e[4] = {f[t].x, f[t].y, f[t].z, f[t].w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) key[t][c] = 4 * v + c < n ? score_key(e[c]) : 0u;
+        for (int c = 0; c < 4; ++c) key[t][c] = FULL || 4 * v + c < n ? score_key(e[c]) : 0u;
     }
     uint32_t a1[4] = {0u, 0u, 0u, 0u}, a2[4] = {0u, 0u, 0u, 0u};   // one top-2 per component
 #pragma unroll
@@ -86,7 +87,9 @@ __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int l
 template <int NV>
 __device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
-    return warp_top_regs<NV>([&](int v) { return r4[v]; }, n, k, lo, buf, dst);
+    auto load4 = [&](int v) { return r4[v]; };
+    return n == 128 * NV ? warp_top_regs<NV, true>(load4, n, k, lo, buf, dst)
+                         : warp_top_regs<NV>(load4, n, k, lo, buf, dst);
 }
 
 __device__ __forceinline__ bool stage_a_smem(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
