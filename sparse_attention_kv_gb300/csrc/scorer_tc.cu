@@ -471,6 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sbuf = reinterpret_cast<float *>(smem + L::offCtrl + sizeof(Ctrl) + kHistBytes);  // FUSED only
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // A dependent grid (the top-k of a chained select) launches once every CTA of this
+    // grid has executed this or exited, so no scorer CTA is still waiting for an SM
+    // when top-k CTAs take free ones; they wait at entry until this grid completes.
+    allow_dependent_launch();
     const int g = blockIdx.y;
     const int q0 = g * p.qg;
     const int qv = min(p.qg, p.nq - q0);  // queries of this group
@@ -677,10 +681,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    // A dependent grid (the top-k of a chained select) starts once every CTA of this
-    // grid has passed this point or exited, so no scorer CTA can still be waiting for
-    // the SM a waiting top-k CTA takes.
-    allow_dependent_launch();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
