@@ -435,9 +435,9 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
 // (more than 64 entries at a chunk's bound) take the radix warp select for that
 // chunk instead.
 
-constexpr int kWarpChunk = 1024;
+constexpr int kWarpChunk = 1024;   // blocks per warp (CL); 512-block chunks measured slower even for 3 queries
 
-template <int NW>
+template <int NW, int CL>
 __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
     __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
@@ -455,17 +455,17 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     uint64_t *buf = reinterpret_cast<uint64_t *>(h);
     for (int i = lane; i < 256; i += 32) h[i] = 0u;
     __syncwarp();
-    const int lo = warp * kWarpChunk;
-    const int len = min(kWarpChunk, n - lo);
+    const int lo = warp * CL;
+    const int len = min(CL, n - lo);
     uint64_t *dst = lists + warp * k;
     if (len > k) {
         const float *r = row + lo;
         const float4 *r4 = reinterpret_cast<const float4 *>(r);
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
         const bool ok =
-            vec && len == kWarpChunk
-                ? warp_top_regs<kWarpChunk / 128, true>([&](int v) { return __ldcs(r4 + v); }, len, k, lo, buf, dst)
-                : warp_top_regs<kWarpChunk / 128>(
+            vec && len == CL
+                ? warp_top_regs<CL / 128, true>([&](int v) { return __ldcs(r4 + v); }, len, k, lo, buf, dst)
+                : warp_top_regs<CL / 128>(
                       [&](int v) {
                           if (vec && 4 * v + 3 < len) return __ldcs(r4 + v);
                           float e[4];
@@ -496,8 +496,8 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     // above it (a binary search); packed values are distinct, so the ranks are a
     // permutation and exactly k candidates rank below k.  One thread per candidate.
     __shared__ int32_t sel[32];
-    const int nch = (n + kWarpChunk - 1) / kWarpChunk;
-    auto cnt_of = [&](int c) { return c < nch ? min(k, n - c * kWarpChunk) : 0; };
+    const int nch = (n + CL - 1) / CL;
+    auto cnt_of = [&](int c) { return c < nch ? min(k, n - c * CL) : 0; };
     if (lane < cnt_of(warp)) {
         const uint64_t x = lists[warp * k + lane];
         int rank = lane;
@@ -564,14 +564,17 @@ qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) { return launch
 qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s) {
     if (a.k > 32)
         return fail(QSA_ERR_UNSUPPORTED, "warp path takes k <= 32 (got %d)", a.k);
+    if (a.bound > 8 * kWarpChunk)
+        return fail(QSA_ERR_UNSUPPORTED, "warp path holds at most %d blocks per row (bound %d)", 8 * kWarpChunk,
+                    a.bound);
     const char *what = "topk_warp_kernel launch";
     const dim3 grid(a.nq);
-    if (a.bound <= kWarpChunk) return launch_dependent(what, topk_warp_kernel<1>, grid, dim3(32), s, a);
-    if (a.bound <= 2 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<2>, grid, dim3(64), s, a);
-    if (a.bound <= 4 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<4>, grid, dim3(128), s, a);
-    if (a.bound <= 8 * kWarpChunk) return launch_dependent(what, topk_warp_kernel<8>, grid, dim3(256), s, a);
-    return fail(QSA_ERR_UNSUPPORTED, "warp path holds at most %d blocks per row (bound %d)", 8 * kWarpChunk,
-                a.bound);
+    if (a.bound <= kWarpChunk) return launch_dependent(what, topk_warp_kernel<1, kWarpChunk>, grid, dim3(32), s, a);
+    if (a.bound <= 2 * kWarpChunk)
+        return launch_dependent(what, topk_warp_kernel<2, kWarpChunk>, grid, dim3(64), s, a);
+    if (a.bound <= 4 * kWarpChunk)
+        return launch_dependent(what, topk_warp_kernel<4, kWarpChunk>, grid, dim3(128), s, a);
+    return launch_dependent(what, topk_warp_kernel<8, kWarpChunk>, grid, dim3(256), s, a);
 }
 
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s) {

@@ -188,16 +188,18 @@ def test_sample_few_candidates_falls_back(k):
     assert flags & qsa.ERROR_FLAGS == 0
 
 
-@pytest.mark.parametrize("n", [33, 64, 65, 1023, 1024, 1025, 2047, 2048, 4097, 8191, 8192])
+@pytest.mark.parametrize("nq", [4, 160])
+@pytest.mark.parametrize("n", [33, 64, 65, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 4097, 8191, 8192])
 @pytest.mark.parametrize("kind", ["normal", "levels", "equal"])
-def test_warp_path_chunk_boundaries(n, kind):
-    """Rows that end inside, at and just past a warp's 1,024-block chunk, with continuous,
-    quantised and all-equal scores (the last two take the radix fallbacks)."""
-    nq, C, k = 4, 8192, 32
+def test_warp_path_chunk_boundaries(nq, n, kind):
+    """Rows that end inside, at and just past a warp's 1,024-block chunk (and half of it),
+    for a few and for many queries, with continuous, quantised and all-equal scores (the
+    last two take the radix fallbacks)."""
+    C, k = 8192, 32
     seed = 6900 + n
     sc = (inputs.normal_scores(seed, nq, C) if kind == "normal" else
           inputs.level_scores(seed, nq, C) if kind == "levels" else np.full((nq, C), 0.5, dtype=np.float32))
-    nb = np.array([n, max(n - 1, 0), min(n + 1, C), n], dtype=np.int32)
+    nb = np.resize(np.array([n, max(n - 1, 0), min(n + 1, C), n], dtype=np.int32), nq)
     ids, flags, _ = run_topk(sc, nb, k, qsa.PATH_WARP, active=C)
     np.testing.assert_array_equal(ids, oracle.select_f32(sc, nb, k))
     assert flags & qsa.ERROR_FLAGS == 0
