@@ -131,3 +131,29 @@ def test_select_is_deterministic():
     b = run_select(case)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("nq,H", [(100, 16), (200, 8)])
+def test_scorer_many_groups_partial_group_ragged_and_clamped(nq, H):
+    """Many query groups with a partial last one, contexts from 0 to the full 8,192 blocks
+    and two out of range: scores against FP64 (rule b), untouched past n, the clamp
+    flag raised."""
+    C = 8192
+    toks = inputs.ragged_tokens(7300 + nq, nq, C)
+    toks[:6] = [0, 64, 64 * 128, 64 * 128 + 1, 64 * C, 64 * C - 63]
+    case = inputs.make_case(7300 + nq + H, nq, H, C, inputs.BF16, toks, 32, active_blocks=C)
+    q, w, kb, nb = parity.to_device(case)
+    nb[7] = C + 500      # past the bound: clamped to it
+    nb[8] = -4           # negative: clamped to 0
+    sc = torch.full((nq, C), float("nan"), dtype=torch.float32, device="cuda")
+    ws = qsa.alloc_workspace(nq, C, 32)
+    qsa.block_scores(q, w, kb, nb, sc, active_blocks=C, ws=ws)
+    flags = qsa.read_flags(ws)
+    assert flags & qsa.FLAG_NBLOCKS_CLAMPED
+    assert flags & qsa.FLAG_WAIT_TIMEOUT == 0
+    n_eff = np.clip(nb.cpu().numpy(), 0, C)
+    got = sc.cpu().numpy()
+    ref = oracle.block_scores(case.q, case.w, case.kblk, n_eff, case.dtype)
+    parity.check_rule_b(got, ref, n_eff, case.dtype)
+    for qi, n in enumerate(n_eff):
+        assert np.isnan(got[qi, n:]).all()
