@@ -1,13 +1,15 @@
-// warp_topk.cuh -- one warp's exact top-k (k <= 32) of a query's scores held in
-// shared memory, the selection step of the fused score-then-select kernel.
+// warp_topk.cuh -- one warp's exact top-k (k <= 32) of a chunk of a query's scores,
+// and the merge of chunks' top-k lists: the selection steps of the warp top-k path
+// (rows read from HBM) and of the fused score-then-select kernel (rows in shared
+// memory).
 //
 // The selection is the one of "#2093 sm_75: the prompt path's top-k with one
 // full read of the scores" (description, step 3): the k largest keys, ties
 // to the lower block id.  Candidates travel packed as (key << 32) | ~id, so a
-// larger packed value is exactly "taken first".  Both forms bound the k-th
+// larger packed value is exactly "taken first".  Each step bounds the k-th
 // largest key from below with a few keys that are provably distinct entries,
-// keep only the entries at or above the bound (a few more than k on continuous
-// scores) and rank those exactly; heavy ties (more than 64 survivors) report
+// keeps only the entries at or above the bound (a few more than k on continuous
+// scores) and ranks those exactly; heavy ties (more than 64 survivors) report
 // failure and the caller falls back to the radix warp select.
 #pragma once
 
@@ -15,18 +17,16 @@
 
 namespace qsa {
 
-// Stage A of one query on one CTA, fast form (k <= 32): the exact top-k of the
-// CTA's n > k scores of the query (row[0..n), block ids lo + i), written to
-// dst[0..k) as packed candidates in descending order.  Each lane keeps the two
-// largest keys of its share, the k-th largest of those 64 bounds the answer from
-// below, the keys at or above it (about k + 4 on continuous scores) are gathered
-// into buf at offsets from one warp scan of the lanes' counts, and their exact
-// ranks pick the top k.  Rows of up to 32 * 4 * NV scores are held in registers
-// (one read of shared memory); longer rows are read three times.  Returns false,
-// having written nothing, when more than 64 keys reach the bound (heavy ties).
-// load4(v) returns row entries 4v .. 4v + 3 (called for 4v < n; entries at or past
-// n may hold anything).  FULL: the caller guarantees n == 128 * NV, and no entry is
-// tested against n.
+// The exact top-k (k <= 32) of a chunk of n > k scores (block ids lo + i), written
+// to dst[0..k) as packed candidates in descending order, the chunk held in registers
+// (n <= 128 * NV, one read).  Each lane keeps the two largest keys of its share; the
+// k-th largest of those 64 bounds the answer from below; the keys at or above it
+// (about k + 4 on continuous scores) are gathered into buf (64 entries) at offsets
+// from one warp scan of the lanes' counts, and their exact ranks pick the top k.
+// Returns false, having written nothing, when more than 64 keys reach the bound
+// (heavy ties) or fewer than k of the 64 keys are nonzero.  load4(v) returns entries
+// 4v .. 4v + 3 (called for 4v < n; entries at or past n may hold anything).  FULL:
+// the caller guarantees n == 128 * NV, and no entry is tested against n.
 template <int NV, bool FULL = false, typename Load4>
 __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const int lane = threadIdx.x & 31;
@@ -92,6 +92,8 @@ __device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int
                          : warp_top_regs<NV>(load4, n, k, lo, buf, dst);
 }
 
+// The same selection for shared-memory rows too long for registers: the row is read
+// three times (top-2, count, gather) instead of once.
 __device__ __forceinline__ bool stage_a_smem(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const int lane = threadIdx.x & 31;
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
