@@ -268,6 +268,51 @@ def cpu_baseline(case, target_s=10.0):
                       f"FP64 scores + full sort, single thread, scaled to the full call"}
 
 
+def cpu_baseline_all_cores(case, target_s=6.0):
+    """The same oracle over every host core: threads take 4-query slices (the oracle's C
+    calls release the GIL) until the time is up; wall time per query, scaled to the call."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.build()
+    cores = os.cpu_count() or 1
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t_start = time.perf_counter()
+
+    def worker():
+        while time.perf_counter() - t_start < target_s:
+            with lock:
+                lo = state["next"] % case.nq
+                state["next"] += 4
+            sl = slice(lo, min(lo + 4, case.nq))
+            s = oracle.block_scores(case.q[sl], case.w[sl], case.kblk, case.n_blocks[sl], case.dtype)
+            oracle.select(s, case.n_blocks[sl], case.k)
+            with lock:
+                state["done"] += sl.stop - sl.start
+
+    with ThreadPoolExecutor(cores) as ex:
+        for f in [ex.submit(worker) for _ in range(cores)]:
+            f.result()
+    wall = time.perf_counter() - t_start
+    return {"value": wall / state["done"] * case.nq * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{state['done']} queries of the same workload over {cores} threads in {wall:.1f} s, "
+                      f"scaled to the full call"}
+
+
+def warm_us_per_call(torch, fn, calls, stream):
+    """Back-to-back calls between one event pair (no flush): steady-state us per call."""
+    fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.Event(enable_timing=True)
+    en = torch.cuda.Event(enable_timing=True)
+    st.record(stream)
+    for _ in range(calls):
+        fn()
+    en.record(stream)
+    torch.cuda.synchronize()
+    return st.elapsed_time(en) * 1e3 / calls
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -405,6 +450,27 @@ def run_ours(args):
     t_dec_f = timed_loop(torch, decode_fused, reps, flush, stream)
     t_dec_c = timed_loop(torch, decode_chained, reps, flush, stream)
     t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream, prime=False)
+    # every top-k path forced on the same deep and decode scores (cold), and both select
+    # forms back to back (warm)
+    topk_paths = {}
+    for name, pth, cs, sc_, nb_, ids_, ws_, act in (
+            ("deep", None, case, scores, nb, ids, ws, case.active_blocks),
+            ("decode", None, dcase, dscores, dnb, dids, dws, -1)):
+        select_chained() if name == "deep" else decode_chained()
+        res = {}
+        for pth in (qsa.PATH_WARP, qsa.PATH_SAMPLE, qsa.PATH_REGISTER, qsa.PATH_SPLIT, qsa.PATH_RADIX):
+            fn = (lambda p_=pth, c_=cs, s_=sc_, n_=nb_, i_=ids_, w_=ws_, a_=act:
+                  qsa.block_topk(s_, n_, c_.k, i_, w_, active_blocks=a_, path=p_))
+            try:
+                fn()
+            except qsa.QSAError:
+                continue
+            res[qsa.PATH_NAMES[pth]] = statistics.median(timed_loop(torch, fn, 50, flush, stream)) * 1e3
+        topk_paths[name] = res
+    warm = {"deep_chained": warm_us_per_call(torch, select_chained, 200, stream),
+            "deep_fused": warm_us_per_call(torch, select_fused, 200, stream),
+            "decode_chained": warm_us_per_call(torch, decode_chained, 200, stream),
+            "decode_fused": warm_us_per_call(torch, decode_fused, 200, stream)}
     clocks = sampler.stop()
 
     ms_main = max_over_ranks(statistics.mean(t_main), device=dev)
@@ -463,12 +529,15 @@ def run_ours(args):
                            "frac_of_hbm": dec_bytes / (us_dec * 1e-6) / 1e9 / peaks["hbm_gbs"]},
         "e2e": {"value": us_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "form": form},
+        "topk_paths_us_cold": topk_paths,
+        "warm_back_to_back_us_per_call": warm,
         "gpu_launches": args.steps * (1 if form == "fused" else 1 + topk_launches),
         "clocks": clocks,
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"]},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(case, min(args.cpu_seconds, 6.0))
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
