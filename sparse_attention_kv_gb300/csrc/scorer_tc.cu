@@ -763,13 +763,24 @@ qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KPar
                         cudaStream_t s) {
     constexpr int bytes = smem_bytes<F32, FUSED>();
     static_assert(bytes <= 227 * 1024, "scorer shared memory");
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(scorer_tc_kernel<F32, H, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        bytes);
-    });
-    if (attr_err != cudaSuccess) return check_cuda(attr_err, "cudaFuncSetAttribute(scorer)");
+    // the shared-memory opt-in is a per-device property of the function: set it once on
+    // every device this instantiation launches on
+    static std::mutex mu;
+    static bool opted_in[64] = {false};
+    int dev = 0;
+    qsa_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != QSA_OK) return st;
+    if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!opted_in[dev]) {
+            st = check_cuda(cudaFuncSetAttribute(scorer_tc_kernel<F32, H, FUSED>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                            "cudaFuncSetAttribute(scorer)");
+            if (st != QSA_OK) return st;
+            opted_in[dev] = true;
+        }
+    }
     scorer_tc_kernel<F32, H, FUSED><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
     return check_cuda(cudaGetLastError(), FUSED ? "fused scorer+select launch" : "scorer_tc_kernel launch");
 }
