@@ -153,7 +153,7 @@ static TopkArgs make_topk_args(const float *scores, int64_t stride, const int32_
 
 static qsa_status run_topk(const float *scores, int64_t stride, const int32_t *n_blocks, int nq,
                            int max_blocks, int active_blocks, int k, int32_t *ids, void *ws,
-                           qsa_path path, cudaStream_t s) {
+                           qsa_path path, cudaStream_t s, bool behind_scorer = false) {
     const int bound = effective_bound(max_blocks, active_blocks);
     const WsLayout L = ws_layout(nq, max_blocks, k);
     const TopkArgs a = make_topk_args(scores, stride, n_blocks, nq, bound, k, ids, ws, L);
@@ -173,7 +173,7 @@ static qsa_status run_topk(const float *scores, int64_t stride, const int32_t *n
     case QSA_PATH_RADIX:
         return launch_topk_radix(a, false, s);
     case QSA_PATH_WARP:
-        return launch_topk_warp(a, s);
+        return launch_topk_warp(a, behind_scorer, s);
     default:
         return fail(QSA_ERR_INVALID_ARG, "bad path %d", (int)path);
     }
@@ -282,7 +282,7 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
     st = qsa_block_scores(q, w, kblk, dt, n_blocks, nq, n_heads, head_dim, max_blocks, active_blocks,
                           scores, scores_stride, ws, ws_bytes, stream);
     if (st != QSA_OK) return st;
-    return run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ids, ws, path, s);
+    return run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ids, ws, path, s, true);
 }
 
 qsa_status qsa_read_flags(void *ws, uint32_t *flags, int clear, qsa_stream stream) {

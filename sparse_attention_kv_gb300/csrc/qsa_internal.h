@@ -68,7 +68,9 @@ SplitGeom split_geometry(int bound, int nq, int k, int maxch);
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s);
 qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s);
 qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s);
-qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s);
+// behind_scorer: the top-k follows the scorer of a chained select on the stream (its
+// CTAs are launched early and wait on the SMs the scorer leaves free)
+qsa_status launch_topk_warp(const TopkArgs &a, bool behind_scorer, cudaStream_t s);
 qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s);
 
 struct ScorerArgs {

@@ -21,6 +21,7 @@
 //    selected block is among its chunk's candidates (Strata PR #3987,
 //    "Approach").
 #include <algorithm>
+#include <mutex>
 #include <cstdio>
 
 #include "qsa_device.cuh"
@@ -436,6 +437,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
 // chunk instead.
 
 constexpr int kWarpChunk = 1024;   // blocks per warp (CL); 512-block chunks measured slower even for 3 queries
+constexpr size_t kWarpTwoPerSmBytes = 90 * 1024;   // dynamic shared memory that leaves room for two CTAs per SM
 
 template <int NW, int CL>
 __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
@@ -462,18 +464,19 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
         const float *r = row + lo;
         const float4 *r4 = reinterpret_cast<const float4 *>(r);
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
+        auto load1 = [&](int i) { return __ldg(r + i); };   // the few entries that reach the bound, again
         const bool ok =
             vec && len == CL
-                ? warp_top_regs<CL / 128, true>([&](int v) { return __ldcs(r4 + v); }, len, k, lo, buf, dst)
+                ? warp_top_regs<CL / 128, true>([&](int v) { return __ldg(r4 + v); }, load1, len, k, lo, buf, dst)
                 : warp_top_regs<CL / 128>(
                       [&](int v) {
-                          if (vec && 4 * v + 3 < len) return __ldcs(r4 + v);
+                          if (vec && 4 * v + 3 < len) return __ldg(r4 + v);
                           float e[4];
 #pragma unroll
-                          for (int c = 0; c < 4; ++c) e[c] = 4 * v + c < len ? __ldcs(r + 4 * v + c) : 0.0f;
+                          for (int c = 0; c < 4; ++c) e[c] = 4 * v + c < len ? __ldg(r + 4 * v + c) : 0.0f;
                           return make_float4(e[0], e[1], e[2], e[3]);
                       },
-                      len, k, lo, buf, dst);
+                      load1, len, k, lo, buf, dst);
         if (!ok) {
             for (int i = lane; i < 256; i += 32) h[i] = 0u;
             __syncwarp();
@@ -531,11 +534,11 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
 // that kernel drains and wait at entry until it has completed.
 template <typename... KArgs, typename... Args>
 static qsa_status launch_dependent(const char *what, void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
-                                   Args... args) {
+                                   size_t dyn_smem, Args... args) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = dyn_smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -549,10 +552,10 @@ template <bool SAMPLE>
 static qsa_status launch_row(const TopkArgs &a, cudaStream_t s) {
     const char *what = SAMPLE ? "topk_row_kernel<sample> launch" : "topk_row_kernel launch";
     const dim3 grid(a.nq), block(kNT);
-    if (a.bound <= 1024) return launch_dependent(what, topk_row_kernel<1, SAMPLE>, grid, block, s, a);
-    if (a.bound <= 2048) return launch_dependent(what, topk_row_kernel<2, SAMPLE>, grid, block, s, a);
-    if (a.bound <= 4096) return launch_dependent(what, topk_row_kernel<4, SAMPLE>, grid, block, s, a);
-    if (a.bound <= kRegisterCap) return launch_dependent(what, topk_row_kernel<8, SAMPLE>, grid, block, s, a);
+    if (a.bound <= 1024) return launch_dependent(what, topk_row_kernel<1, SAMPLE>, grid, block, s, 0, a);
+    if (a.bound <= 2048) return launch_dependent(what, topk_row_kernel<2, SAMPLE>, grid, block, s, 0, a);
+    if (a.bound <= 4096) return launch_dependent(what, topk_row_kernel<4, SAMPLE>, grid, block, s, 0, a);
+    if (a.bound <= kRegisterCap) return launch_dependent(what, topk_row_kernel<8, SAMPLE>, grid, block, s, 0, a);
     return fail(QSA_ERR_UNSUPPORTED, "%s path holds at most %d blocks per row (bound %d)",
                 SAMPLE ? "sample" : "register", kRegisterCap, a.bound);
 }
@@ -561,7 +564,7 @@ qsa_status launch_topk_register(const TopkArgs &a, cudaStream_t s) { return laun
 
 qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s) { return launch_row<true>(a, s); }
 
-qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s) {
+qsa_status launch_topk_warp(const TopkArgs &a, bool behind_scorer, cudaStream_t s) {
     if (a.k > 32)
         return fail(QSA_ERR_UNSUPPORTED, "warp path takes k <= 32 (got %d)", a.k);
     if (a.bound > 8 * kWarpChunk)
@@ -569,16 +572,37 @@ qsa_status launch_topk_warp(const TopkArgs &a, cudaStream_t s) {
                     a.bound);
     const char *what = "topk_warp_kernel launch";
     const dim3 grid(a.nq);
-    if (a.bound <= kWarpChunk) return launch_dependent(what, topk_warp_kernel<1, kWarpChunk>, grid, dim3(32), s, a);
+    if (a.bound <= kWarpChunk) return launch_dependent(what, topk_warp_kernel<1, kWarpChunk>, grid, dim3(32), s, 0, a);
     if (a.bound <= 2 * kWarpChunk)
-        return launch_dependent(what, topk_warp_kernel<2, kWarpChunk>, grid, dim3(64), s, a);
+        return launch_dependent(what, topk_warp_kernel<2, kWarpChunk>, grid, dim3(64), s, 0, a);
     if (a.bound <= 4 * kWarpChunk)
-        return launch_dependent(what, topk_warp_kernel<4, kWarpChunk>, grid, dim3(128), s, a);
-    return launch_dependent(what, topk_warp_kernel<8, kWarpChunk>, grid, dim3(256), s, a);
+        return launch_dependent(what, topk_warp_kernel<4, kWarpChunk>, grid, dim3(128), s, 0, a);
+    if (!behind_scorer) return launch_dependent(what, topk_warp_kernel<8, kWarpChunk>, grid, dim3(256), s, 0, a);
+    // Behind the scorer, at most two of these 8-warp CTAs per SM (an otherwise unused
+    // shared-memory reservation): the CTAs launched early wait on the SMs the scorer
+    // leaves free, and three to such an SM make it finish last (deep prompt select
+    // 26.9 us with three, 24.9 with two; the top-k alone prefers three, 12.4 us to 13.7).
+    static std::mutex mu;
+    static bool opted_in[64] = {false};
+    int dev = 0;
+    qsa_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != QSA_OK) return st;
+    if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!opted_in[dev]) {
+            st = check_cuda(cudaFuncSetAttribute(topk_warp_kernel<8, kWarpChunk>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWarpTwoPerSmBytes),
+                            "cudaFuncSetAttribute(topk_warp_kernel)");
+            if (st != QSA_OK) return st;
+            opted_in[dev] = true;
+        }
+    }
+    return launch_dependent(what, topk_warp_kernel<8, kWarpChunk>, grid, dim3(256), s, kWarpTwoPerSmBytes, a);
 }
 
 qsa_status launch_topk_radix(const TopkArgs &a, bool flagged_only, cudaStream_t s) {
-    return launch_dependent("topk_radix_kernel launch", topk_radix_kernel<512>, dim3(a.nq), dim3(512), s, a,
+    return launch_dependent("topk_radix_kernel launch", topk_radix_kernel<512>, dim3(a.nq), dim3(512), s, 0, a,
                             flagged_only ? 1 : 0);
 }
 
@@ -604,7 +628,7 @@ SplitGeom split_geometry(int bound, int nq, int k, int maxch) {
 qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s) {
     if (g.chunk_len <= 0 || g.chunk_len > kSplitMaxChunk)
         return fail(QSA_ERR_UNSUPPORTED, "split path: no chunk geometry fits (bound %d, k %d)", a.bound, a.k);
-    return launch_dependent("topk_split_kernel launch", topk_split_kernel, dim3(g.nchunks, a.nq), dim3(kNT), s, a,
+    return launch_dependent("topk_split_kernel launch", topk_split_kernel, dim3(g.nchunks, a.nq), dim3(kNT), s, 0, a,
                             g.chunk_len);
 }
 

@@ -25,10 +25,13 @@ namespace qsa {
 // from one warp scan of the lanes' counts, and their exact ranks pick the top k.
 // Returns false, having written nothing, when more than 64 keys reach the bound
 // (heavy ties) or fewer than k of the 64 keys are nonzero.  load4(v) returns entries
-// 4v .. 4v + 3 (called for 4v < n; entries at or past n may hold anything).  FULL:
-// the caller guarantees n == 128 * NV, and no entry is tested against n.
-template <int NV, bool FULL = false, typename Load4>
-__device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
+// 4v .. 4v + 3 (called for 4v < n; entries at or past n may hold anything); load1(i)
+// returns entry i again for the few that reach the bound.  FULL: the caller
+// guarantees n == 128 * NV, and no entry is tested against n.
+template <int NV, bool FULL = false, typename Load4, typename Load1>
+__device__ __forceinline__ bool warp_top_regs(Load4 &&load4, Load1 &&load1, int n, int k, int lo, uint64_t *buf,
+                                              uint64_t *dst) {
+    static_assert(NV * 4 <= 32, "one survivor bit per entry of a lane");
     const int lane = threadIdx.x & 31;
     // every load in flight before the first use
     float4 f[NV];
@@ -63,20 +66,23 @@ __device__ __forceinline__ bool warp_top_regs(Load4 &&load4, int n, int k, int l
     // nonzero keys among the 64) gives no filter
     const uint32_t lb = warp_bound_from_top2(m1, m2, k);
     if (lb == 0u) return false;
-    int nk = 0;
-#pragma unroll
-    for (int t = 0; t < NV; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) nk += key[t][c] >= lb;
-    const int incl = warp_incl_scan(nk);
-    const int m = __shfl_sync(kFull, incl, 31);
-    if (m > 64) return false;
-    int pos = incl - nk;
+    uint32_t surv = 0u;   // bit 4t + c: entry (t, c) of this lane reaches the bound
 #pragma unroll
     for (int t = 0; t < NV; ++t)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            if (key[t][c] >= lb) buf[pos++] = pack_cand(key[t][c], lo + 4 * (lane + 32 * t) + c);
+            if (key[t][c] >= lb) surv |= 1u << (4 * t + c);
+    const int nk = __popc(surv);
+    const int incl = warp_incl_scan(nk);
+    const int m = __shfl_sync(kFull, incl, 31);
+    if (m > 64) return false;
+    int pos = incl - nk;
+    while (surv) {   // about one survivor per lane: read it again rather than test every entry
+        const int bit = __ffs(surv) - 1;
+        surv &= surv - 1u;
+        const int i = 4 * (lane + 32 * (bit >> 2)) + (bit & 3);
+        buf[pos++] = pack_cand(score_key(load1(i)), lo + i);
+    }
     __syncwarp();
     warp_rank_top(buf, m, k, [&](int r, uint64_t c) { dst[r] = c; });
     return true;
@@ -88,8 +94,9 @@ template <int NV>
 __device__ __forceinline__ bool stage_a_regs(const float *row, int n, int k, int lo, uint64_t *buf, uint64_t *dst) {
     const float4 *r4 = reinterpret_cast<const float4 *>(row);
     auto load4 = [&](int v) { return r4[v]; };
-    return n == 128 * NV ? warp_top_regs<NV, true>(load4, n, k, lo, buf, dst)
-                         : warp_top_regs<NV>(load4, n, k, lo, buf, dst);
+    auto load1 = [&](int i) { return row[i]; };
+    return n == 128 * NV ? warp_top_regs<NV, true>(load4, load1, n, k, lo, buf, dst)
+                         : warp_top_regs<NV>(load4, load1, n, k, lo, buf, dst);
 }
 
 // The same selection for shared-memory rows too long for registers: the row is read
