@@ -371,26 +371,34 @@ def run_ours(args):
     def decode_fused():
         qsa.select(dq, dw, dkb, dnb, dcase.k, dids, dfws, fused=True, active_blocks=-1)
 
-    # end to end: pinned host inputs -> device, select, ids -> pinned host
-    hq = q.cpu().pin_memory()
-    hw = w.cpu().pin_memory()
-    hkb = kb.cpu().pin_memory()
-    hnb = nb.cpu().pin_memory()
+    # end to end: the step's inputs (q, w, kblk, n_blocks) staged in one pinned host
+    # buffer in 256-byte aligned sections, one host-to-device copy, the call on views of
+    # the device copy, and the ids read back to pinned host memory
+    sections = (q, w, kb, nb)
+    offs, total = [], 0
+    for t in sections:
+        total = (total + 255) // 256 * 256
+        offs.append(total)
+        total += t.numel() * t.element_size()
+    hstage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dstage = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(sections, offs):
+        nbytes = t.numel() * t.element_size()
+        hstage[o:o + nbytes].copy_(t.cpu().contiguous().view(torch.uint8).reshape(-1))
+        views.append(dstage[o:o + nbytes].view(t.dtype).view(t.shape))
+    eq_, ew_, ekb_, enb_ = views
     hids = torch.empty_like(ids, device="cpu").pin_memory()
-    eq_, ew_, ekb_, enb_ = (torch.empty_like(t) for t in (q, w, kb, nb))
 
     def e2e_step():
-        eq_.copy_(hq, non_blocking=True)
-        ew_.copy_(hw, non_blocking=True)
-        ekb_.copy_(hkb, non_blocking=True)
-        enb_.copy_(hnb, non_blocking=True)
+        dstage.copy_(hstage, non_blocking=True)
         if form == "fused":
             qsa.select(eq_, ew_, ekb_, enb_, case.k, ids, fws, fused=True, active_blocks=case.active_blocks)
         else:
             qsa.select(eq_, ew_, ekb_, enb_, case.k, ids, ws, scores=scores, active_blocks=case.active_blocks)
         hids.copy_(ids, non_blocking=True)
 
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hw, hkb, hnb))
+    h2d = sum(t.numel() * t.element_size() for t in sections)
     d2h = hids.numel() * hids.element_size()
 
     form = "fused"
