@@ -157,3 +157,22 @@ def test_scorer_many_groups_partial_group_ragged_and_clamped(nq, H):
     parity.check_rule_b(got, ref, n_eff, case.dtype)
     for qi, n in enumerate(n_eff):
         assert np.isnan(got[qi, n:]).all()
+
+
+def test_fp32_inputs_at_scale_chained_and_fused():
+    """fp32 q and kblk (the three-term TF32 split) at 64 queries x 2,048 blocks with ragged
+    contexts: scores within 1e-4 of FP64 (rule b), ids by rules (a) and (c), and the fused
+    form's ids equal to the chained form's."""
+    nq, C, k = 64, 2048, 32
+    toks = inputs.ragged_tokens(7400, nq, C)
+    case = inputs.make_case(7400, nq, 16, C, inputs.F32, toks, k, active_blocks=C)
+    ids, sc, r = full_check(case)
+    ids_f, _, flags = run_select(case, fused=True)
+    assert flags & qsa.ERROR_FLAGS == 0
+    np.testing.assert_array_equal(ids_f, ids)
+
+
+@pytest.mark.parametrize("path", [qsa.PATH_WARP, qsa.PATH_SAMPLE, qsa.PATH_REGISTER, qsa.PATH_RADIX])
+def test_every_path_end_to_end_on_the_deep_prompt(path):
+    """The 256-query, 520,000-token prompt through each top-k path that holds its rows."""
+    full_check(inputs.deep_case(2), path)
