@@ -59,7 +59,6 @@ def workload_config(case):
                     f"{int(case.tokens[0]):,} tokens ({n:,} blocks of 64), k={case.k}, capacity 524,288 tokens",
         "nq": case.nq, "n_heads": case.n_heads, "n_blocks": n, "k": case.k,
         "l2": "flushed before every timed step (256 MB write)",
-        "path": "chained select (tcgen05 scorer -> top-k auto path)",
     }
 
 
@@ -524,7 +523,10 @@ def run_ours(args):
         "metric": METRIC, "value": us_main, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_main, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/kblk, U(0,1) w)",
-        "config": dict(workload_config(case), select_form=form),
+        "config": dict(workload_config(case), select_form=form,
+                       path=("fused select: one tcgen05 scorer kernel that selects on chip" if form == "fused" else
+                             f"chained select: tcgen05 scorer, then the {qsa.PATH_NAMES[path]} top-k path "
+                             "launched as its programmatic dependent")),
         "selections_per_s": case.nq * world / (ms_main * 1e-3),
         "roofline": roof,
         "forms_us_median": {form: us_main_median, ("chained" if form == "fused" else "fused"): us_other},
