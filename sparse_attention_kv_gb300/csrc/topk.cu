@@ -1,6 +1,13 @@
 // topk.cu -- block top-k kernels over fp32 score rows.
 //
-// Four paths, all giving the ids of the rule in qsa_device.cuh:
+// Five paths, all giving the ids of the rule in qsa_device.cuh.  Every kernel is
+// launched as a programmatic dependent of the kernel before it on the stream and
+// waits at entry until that kernel has completed (in a chained select its CTAs
+// take SMs while the scorer drains).
+//  * warp:     k <= 32, rows of up to 8,192 blocks: one CTA per query, one warp
+//    per 1,024-block chunk bounds, filters and ranks its chunk in registers, and
+//    the chunks' lists are merged by exact ranks (warp_topk.cuh); the AUTO choice
+//    wherever it applies.
 //  * register: one CTA per query holds its whole row in registers (<= 8,192
 //    blocks: 256 threads x 32) and selects with no re-read -- the "register
 //    kernel" the pages name for contexts within its reach (Strata PR #3987,
@@ -21,8 +28,8 @@
 //    selected block is among its chunk's candidates (Strata PR #3987,
 //    "Approach").
 #include <algorithm>
-#include <mutex>
 #include <cstdio>
+#include <mutex>
 
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
