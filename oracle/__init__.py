@@ -17,6 +17,11 @@ select(scores, n_blocks, k)
     block id, -1 padded.
 select_f32(scores, n_blocks, k)
     The same selection over float32 scores (e.g. the GPU's own).
+select_attention(qa, kc, vc, ids, n_tokens, scale)
+    Selection attention over the selected blocks in double: per query and
+    head, softmax(scale * q.K^T) V over the tokens of the query's distinct
+    selected blocks below its context length, and the log-sum-exp.  ``qa``
+    [nq,H,D], ``kc``/``vc`` [Hkv,C,D] (token rows) as bf16 bits (uint16).
 
 Parity status: pinned (see the oracle tests).
 """
@@ -46,7 +51,7 @@ def build(force: bool = False) -> str:
         if force or stale:
             tmp = _LIB + f".tmp{os.getpid()}"
             cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-                   "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC]
+                   "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB
@@ -70,6 +75,10 @@ def _load():
         lib.qsa_oracle_select_f32.argtypes = [fp, ctypes.c_int64, i32p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, i32p]
         lib.qsa_oracle_select_f32.restype = ctypes.c_int
+        lib.qsa_oracle_select_attention.argtypes = [vp, vp, vp, i32p, ctypes.c_int, i32p, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_double, dp, dp]
+        lib.qsa_oracle_select_attention.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -129,3 +138,28 @@ def select_f32(scores: np.ndarray, n_blocks: np.ndarray, k: int) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle.select_f32: bad argument")
     return ids
+
+
+def select_attention(qa: np.ndarray, kc: np.ndarray, vc: np.ndarray, ids: np.ndarray,
+                     n_tokens: np.ndarray, scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """(out [nq,H,D], lse [nq,H]) in double; qa [nq,H,D], kc/vc [Hkv,C,D], ids [nq,k] int32."""
+    lib = _load()
+    qa = np.ascontiguousarray(qa, dtype=np.uint16)
+    kc = np.ascontiguousarray(kc, dtype=np.uint16)
+    vc = np.ascontiguousarray(vc, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n_tokens = np.ascontiguousarray(n_tokens, dtype=np.int32)
+    nq, H, D = qa.shape
+    Hkv, C, Dk = kc.shape
+    k = ids.shape[1]
+    if vc.shape != kc.shape or Dk != D or ids.shape[0] != nq or n_tokens.shape != (nq,):
+        raise ValueError("oracle.select_attention: shape mismatch")
+    out = np.zeros((nq, H, D), dtype=np.float64)
+    lse = np.zeros((nq, H), dtype=np.float64)
+    rc = lib.qsa_oracle_select_attention(qa.ctypes.data, kc.ctypes.data, vc.ctypes.data,
+                                         _ptr(ids, ctypes.c_int32), int(k), _ptr(n_tokens, ctypes.c_int32),
+                                         nq, H, Hkv, D, C, float(scale), _ptr(out, ctypes.c_double),
+                                         _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle.select_attention: bad argument")
+    return out, lse

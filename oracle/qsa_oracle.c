@@ -26,6 +26,9 @@
  * key (score desc, id asc) is a total order, so the result is the same as a
  * stable sort by score of the blocks listed in id order.
  *
+ * The third function, selection attention over the selected blocks, is
+ * described above its definition.
+ *
  * Parity status: pinned.  The pins (hand-computed fixtures, closed forms,
  * exact-sum cross checks, brute force over all k-subsets) live in the tests.
  *
@@ -35,6 +38,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 
@@ -163,5 +167,94 @@ int qsa_oracle_select_f32(const float *scores, int64_t stride, const int32_t *n_
         }
     }
     free(row);
+    return 0;
+}
+
+/*
+ * Selection attention, forward, in double: the step that consumes the selected
+ * ids, as set out in "[wave] NSA: LDS optimization for block-gather in
+ * selection attention" (section "Problem": each query reads the tokens of its
+ * selected blocks, T blocks of block_size tokens; strategy 1: the heads of a
+ * GQA group read one copy of each block's K and V).  For query qi and attention
+ * head h, whose KV head is g = h / group:
+ *
+ *   tokens   the set of t = 64 * b + r over the distinct ids b >= 0 of
+ *            ids[qi][0..k) and 0 <= r < 64, with t < min(n_tokens[qi], capacity)
+ *   logits   s_t = scale * sum_d qa[qi][h][d] * kc[g][t][d]
+ *   out      o[qi][h][d] = sum_t exp(s_t - m) * vc[g][t][d] / sum_t exp(s_t - m),
+ *            m = max_t s_t
+ *   lse      lse[qi][h] = m + log(sum_t exp(s_t - m))
+ *
+ * The tokens are visited in slot order; an empty set gives o = 0 and
+ * lse = -inf.  Inputs are bf16 bit patterns, widened exactly; everything after
+ * that is IEEE double.  qa: [nq][n_heads][head_dim]; kc, vc:
+ * [n_kv_heads][capacity][head_dim] (token rows); ids: [nq][k];
+ * out: [nq][n_heads][head_dim]; lse: [nq][n_heads].
+ * Returns 0, or -1 on a bad argument.
+ */
+int qsa_oracle_select_attention(const uint16_t *qa, const uint16_t *kc, const uint16_t *vc,
+                                const int32_t *ids, int k, const int32_t *n_tokens, int nq,
+                                int n_heads, int n_kv_heads, int head_dim, int capacity,
+                                double scale, double *out, double *lse)
+{
+    if (!qa || !kc || !vc || !ids || !n_tokens || !out || !lse) return -1;
+    if (nq < 0 || k <= 0 || n_kv_heads <= 0 || n_heads <= 0 || n_heads % n_kv_heads) return -1;
+    if (head_dim <= 0 || capacity < 0) return -1;
+    const int group = n_heads / n_kv_heads;
+    const size_t max_tok = (size_t)k * 64;
+    int32_t *tok = (int32_t *)malloc(max_tok * sizeof *tok);
+    double *s = (double *)malloc(max_tok * sizeof *s);
+    if (!tok || !s) {
+        free(tok);
+        free(s);
+        return -1;
+    }
+    for (int qi = 0; qi < nq; ++qi) {
+        const int32_t *row = ids + (size_t)qi * k;
+        int ntok = n_tokens[qi] < 0 ? 0 : n_tokens[qi];
+        if (ntok > capacity) ntok = capacity;
+        /* the query's token set, in slot order */
+        int n = 0;
+        for (int j = 0; j < k; ++j) {
+            const int32_t b = row[j];
+            if (b < 0) continue;
+            int seen = 0;
+            for (int i = 0; i < j; ++i) seen |= row[i] == b;
+            if (seen) continue;
+            for (int r = 0; r < 64; ++r) {
+                const int64_t t = (int64_t)b * 64 + r;
+                if (t < ntok) tok[n++] = (int32_t)t;
+            }
+        }
+        for (int h = 0; h < n_heads; ++h) {
+            const int g = h / group;
+            const size_t qrow = ((size_t)qi * n_heads + h) * head_dim;
+            double *o = out + ((size_t)qi * n_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (n == 0) {
+                lse[(size_t)qi * n_heads + h] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int i = 0; i < n; ++i) {
+                const size_t krow = ((size_t)g * capacity + tok[i]) * head_dim;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d) dot += widen(qa, ORACLE_BF16, qrow + d) * widen(kc, ORACLE_BF16, krow + d);
+                s[i] = scale * dot;
+                if (s[i] > m) m = s[i];
+            }
+            double l = 0.0;
+            for (int i = 0; i < n; ++i) {
+                const double e = exp(s[i] - m);
+                const size_t vrow = ((size_t)g * capacity + tok[i]) * head_dim;
+                l += e;
+                for (int d = 0; d < head_dim; ++d) o[d] += e * widen(vc, ORACLE_BF16, vrow + d);
+            }
+            for (int d = 0; d < head_dim; ++d) o[d] /= l;
+            lse[(size_t)qi * n_heads + h] = m + log(l);
+        }
+    }
+    free(tok);
+    free(s);
     return 0;
 }

@@ -169,3 +169,81 @@ def stress_case(kind: str) -> Case:
         return make_case(5003, 256, 16, 2048, BF16, toks, 32, active_blocks=2048,
                          name="stress: per-query contexts 1..2,048 blocks, partial tail")
     raise ValueError(kind)
+
+
+# ----------------------------------------------------------------------------- selection attention
+
+@dataclass
+class AttnCase:
+    """One synthetic selection-attention problem.
+
+    ``qa`` [nq,H,128] and ``kc``/``vc`` [Hkv,C,128] (token rows) hold bf16 bit
+    patterns (uint16) drawn N(0,1); ``ids`` [nq,k] int32 are distinct block ids
+    inside each query's context, ascending, -1 padded; ``n_tokens`` [nq] int32.
+    The heads of a GQA group (``H / Hkv`` of them) share one KV head.
+    """
+    qa: np.ndarray
+    kc: np.ndarray
+    vc: np.ndarray
+    ids: np.ndarray
+    n_tokens: np.ndarray
+    scale: float
+    name: str = ""
+
+    @property
+    def nq(self) -> int:
+        return self.qa.shape[0]
+
+    @property
+    def n_heads(self) -> int:
+        return self.qa.shape[1]
+
+    @property
+    def n_kv_heads(self) -> int:
+        return self.kc.shape[0]
+
+    @property
+    def capacity(self) -> int:
+        return self.kc.shape[1]
+
+    @property
+    def k(self) -> int:
+        return self.ids.shape[1]
+
+
+def random_ids(seed: int, n_blocks, k: int, n_valid=None) -> np.ndarray:
+    """Per query, min(n_valid, n_blocks, k) distinct ids drawn uniformly from
+    [0, n_blocks), ascending, then -1 (the path's output format)."""
+    rng = np.random.default_rng(seed)
+    nb = np.asarray(n_blocks, dtype=np.int64)
+    nv = nb if n_valid is None else np.minimum(np.asarray(n_valid, dtype=np.int64), nb)
+    out = np.full((len(nb), k), -1, dtype=np.int32)
+    for i, (n, v) in enumerate(zip(nb, nv)):
+        m = int(min(v, k))
+        if m > 0:
+            out[i, :m] = np.sort(rng.choice(int(n), size=m, replace=False))
+    return out
+
+
+def make_attention_case(seed: int, nq: int, n_kv_heads: int, capacity_tokens: int, tokens, k: int, *,
+                        group: int = 16, ids: np.ndarray | None = None, n_valid=None,
+                        name: str = "") -> AttnCase:
+    """qa, kc, vc ~ N(0,1) (bf16), contexts ``tokens`` (scalar or per query); the
+    ids are random distinct blocks of each context unless given."""
+    rng = np.random.default_rng(seed)
+    H = n_kv_heads * group
+    qa = to_bf16_bits(rng.standard_normal((nq, H, HEAD_DIM), dtype=np.float32))
+    kc = to_bf16_bits(rng.standard_normal((n_kv_heads, capacity_tokens, HEAD_DIM), dtype=np.float32))
+    vc = to_bf16_bits(rng.standard_normal((n_kv_heads, capacity_tokens, HEAD_DIM), dtype=np.float32))
+    toks = np.broadcast_to(np.asarray(tokens, dtype=np.int64), (nq,)).astype(np.int32)
+    if ids is None:
+        ids = random_ids(seed + 1, blocks_for_tokens(toks), k, n_valid)
+    return AttnCase(qa=qa, kc=kc, vc=vc, ids=np.ascontiguousarray(ids, dtype=np.int32), n_tokens=toks,
+                    scale=HEAD_DIM ** -0.5, name=name)
+
+
+def vcache_blocks_transposed(vc: np.ndarray) -> np.ndarray:
+    """[Hkv, C, D] token rows -> [Hkv, C/64, D, 64]: each 64-token block of V stored
+    dimension-major (the layout the CUDA selection attention reads)."""
+    Hkv, C, D = vc.shape
+    return np.ascontiguousarray(vc.reshape(Hkv, C // BLOCK_TOKENS, BLOCK_TOKENS, D).transpose(0, 1, 3, 2))

@@ -270,7 +270,7 @@ def test_pins_catch_planted_oracle_mistakes(tmp_path, golden_dir, monkeypatch):
         msrc = tmp_path / f"{name}.c"
         msrc.write_text(src.replace(old, new, 1))
         so = tmp_path / f"{name}.so"
-        subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-w", "-o", str(so), str(msrc)], check=True)
+        subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-w", "-o", str(so), str(msrc), "-lm"], check=True)
         monkeypatch.setattr(oracle, "_lib", None)
         monkeypatch.setattr(oracle, "_LIB", str(so))
         monkeypatch.setattr(oracle, "build", lambda force=False: str(so))
