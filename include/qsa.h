@@ -85,6 +85,13 @@ typedef void *qsa_stream; /* a cudaStream_t */
 #define QSA_FLAG_INTERNAL 0x4u        /* an internal consistency check failed */
 #define QSA_FLAG_SAMPLE_FALLBACK 0x8u /* not an error: some query of the sampled filter had too few
                                          or too many candidates and was selected from its whole row */
+#define QSA_FLAG_BAD_ID 0x10u         /* qsa_select_attention skipped an id outside its query's
+                                         context (an id other than -1) */
+
+/* Query heads per KV head (GQA group) of qsa_select_attention. */
+#define QSA_ATTN_GROUP 16
+/* Largest k of qsa_select_attention. */
+#define QSA_ATTN_MAX_K 64
 
 /*
  * Workspace size in bytes for calls with these sizes (any path, fused or not).
@@ -192,6 +199,55 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
                       int active_blocks, int k, int32_t *ids, float *scores,
                       int64_t scores_stride, int fused, void *ws, size_t ws_bytes,
                       qsa_path path, qsa_stream stream);
+
+/*
+ * Selection attention, forward, over the blocks each query selected: the step
+ * that reads the ids, as described in "[wave] NSA: LDS optimization for
+ * block-gather in selection attention" (section "Problem": a query reads the
+ * tokens of its selected blocks; "LDS staging strategies" 1: the heads of a GQA
+ * group read one on-chip copy of each block's K and V).  For query q and
+ * attention head h, with KV head g = h / QSA_ATTN_GROUP:
+ *
+ *   s_t       = dot(qa[q][h][:], K[g][t][:])
+ *   o[q][h]   = sum_t exp(scale (s_t - m)) V[g][t][:] / sum_t exp(scale (s_t - m)),  m = max_t s_t
+ *   lse[q][h] = scale m + log(sum_t exp(scale (s_t - m)))
+ *
+ * over the tokens t = 64 b + r (0 <= r < 64) of the distinct ids b >= 0 of
+ * ids[q][0..k) with t < n_tokens[q].  A query with no such token gets o = 0 and
+ * lse = -inf.
+ *
+ *   qa        [nq][n_heads][128] bf16, row-major, 16-byte aligned
+ *   kcache    [n_kv_heads][capacity][128] bf16 (K[g][t] = token rows), 16-byte aligned
+ *   vcache_t  [n_kv_heads][capacity / 64][128][64] bf16: each 64-token block of V
+ *             stored dimension-major, element [g][b][d][r] = V[g][64 b + r][d];
+ *             16-byte aligned
+ *   ids       [nq][k] int32: block ids (e.g. the ids of qsa_select), -1 = none, in
+ *             any order; an id outside [0, ceil(n_tokens[q] / 64)) is skipped and sets
+ *             QSA_FLAG_BAD_ID; a repeated id counts once
+ *   n_tokens  [nq] int32 on the DEVICE: context length of each query, clamped to
+ *             [0, capacity] (a clamp sets QSA_FLAG_NBLOCKS_CLAMPED)
+ *   out       [nq][n_heads][128] fp32 out
+ *   lse       [nq][n_heads] fp32 out, or NULL
+ *   scale     softmax scale (host float), finite and > 0 (usually 1 / sqrt(128))
+ *   ws        a workspace of at least 256 bytes (its flags word is used), or NULL
+ *             (then device flags are not recorded)
+ *
+ * Arithmetic: the q.k products on the tensor cores (bf16 x bf16 -> fp32); the
+ * weights exp2((s - m) scale log2 e) in fp32, rounded to bf16 for the P.V product
+ * on the tensor cores (bf16 x bf16 -> fp32), and divided by the sum of the
+ * rounded weights.  Tokens at or past n_tokens take no part, whatever their K and
+ * V rows hold.
+ * Errors: QSA_ERR_INVALID_ARG for NULL qa/kcache/vcache_t/ids/n_tokens/out,
+ * nq < 1, head_dim != 128, n_kv_heads < 1, n_heads != QSA_ATTN_GROUP *
+ * n_kv_heads, k outside [1, QSA_ATTN_MAX_K], capacity < 64 or not a multiple of
+ * 64, n_kv_heads * capacity >= 2^30, nq * n_heads >= 2^30, misaligned
+ * qa/kcache/vcache_t, scale not finite or <= 0, ws smaller than 256 bytes or
+ * not 256-byte aligned; QSA_ERR_UNSUPPORTED for a dtype other than QSA_BF16.
+ */
+qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *vcache_t, qsa_dtype dt,
+                                const int32_t *ids, int k, const int32_t *n_tokens, int nq, int n_heads,
+                                int n_kv_heads, int head_dim, int capacity, float scale, float *out,
+                                float *lse, void *ws, size_t ws_bytes, qsa_stream stream);
 
 /*
  * Copy the workspace flags word (QSA_FLAG_* bits) to host `*flags`, waiting for

@@ -285,6 +285,50 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
     return run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ids, ws, path, s, true);
 }
 
+qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *vcache_t, qsa_dtype dt,
+                                const int32_t *ids, int k, const int32_t *n_tokens, int nq, int n_heads,
+                                int n_kv_heads, int head_dim, int capacity, float scale, float *out,
+                                float *lse, void *ws, size_t ws_bytes, qsa_stream stream) {
+    if (!qa || !kcache || !vcache_t || !ids || !n_tokens || !out)
+        return fail(QSA_ERR_INVALID_ARG, "NULL qa, kcache, vcache_t, ids, n_tokens or out");
+    if (nq < 1) return fail(QSA_ERR_INVALID_ARG, "nq must be >= 1 (got %d)", nq);
+    if (head_dim != QSA_HEAD_DIM)
+        return fail(QSA_ERR_INVALID_ARG, "head_dim must be %d (got %d)", QSA_HEAD_DIM, head_dim);
+    if (n_kv_heads < 1 || (long long)n_heads != (long long)QSA_ATTN_GROUP * n_kv_heads)
+        return fail(QSA_ERR_INVALID_ARG, "n_heads must be %d x n_kv_heads (got %d heads, %d KV heads)",
+                    QSA_ATTN_GROUP, n_heads, n_kv_heads);
+    if (k < 1 || k > QSA_ATTN_MAX_K)
+        return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_ATTN_MAX_K, k);
+    if (capacity < 64 || capacity % 64)
+        return fail(QSA_ERR_INVALID_ARG, "capacity must be a positive multiple of 64 (got %d)", capacity);
+    if ((long long)n_kv_heads * capacity >= (1ll << 30))
+        return fail(QSA_ERR_INVALID_ARG, "n_kv_heads * capacity too large");
+    if ((long long)nq * n_heads >= (1ll << 30)) return fail(QSA_ERR_INVALID_ARG, "nq * n_heads too large");
+    if ((reinterpret_cast<uintptr_t>(qa) | reinterpret_cast<uintptr_t>(kcache) |
+         reinterpret_cast<uintptr_t>(vcache_t)) & 15u)
+        return fail(QSA_ERR_INVALID_ARG, "qa, kcache and vcache_t must be 16-byte aligned");
+    if (!(scale > 0.0f) || !(scale <= 3.4e38f)) return fail(QSA_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (ws && (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return fail(QSA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold at least 256 bytes");
+    if (dt != QSA_BF16) return fail(QSA_ERR_UNSUPPORTED, "selection attention takes bf16 inputs only (dtype %d)", dt);
+    AttnArgs a{};
+    a.qa = qa;
+    a.kcache = kcache;
+    a.vcache_t = vcache_t;
+    a.ids = ids;
+    a.k = k;
+    a.n_tokens = n_tokens;
+    a.nq = nq;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.capacity = capacity;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    a.flags = ws ? static_cast<uint32_t *>(ws) : nullptr;
+    return launch_select_attention(a, static_cast<cudaStream_t>(stream));
+}
+
 qsa_status qsa_read_flags(void *ws, uint32_t *flags, int clear, qsa_stream stream) {
     if (!ws || !flags) return fail(QSA_ERR_INVALID_ARG, "NULL workspace or flags");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

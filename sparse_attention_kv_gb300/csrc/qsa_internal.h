@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/qsa.h"
@@ -16,6 +17,10 @@ qsa_status fail(qsa_status st, const char *fmt, ...);
 qsa_status check_cuda(cudaError_t err, const char *what);
 
 int num_sms();  // SM count of the current device (cached per device)
+
+// A 2-D TMA tensor map over a row-major [rows][inner] array (fp32 or bf16), box of
+// 128 bytes x box_rows, 128-byte swizzle; encoded once per (pointer, shape, device).
+qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint32_t inner, uint64_t rows, uint32_t box_rows);
 
 // Candidate slots per (query, chunk) are sized for chunks of at least this many blocks.
 constexpr int kMinChunk = 128;
@@ -95,5 +100,23 @@ struct ScorerArgs {
     int maxch;
 };
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);
+
+struct AttnArgs {
+    const void *qa;
+    const void *kcache;
+    const void *vcache_t;
+    const int32_t *ids;
+    int k;
+    const int32_t *n_tokens;
+    int nq;
+    int n_heads;
+    int n_kv_heads;
+    int capacity;
+    float scale;
+    float *out;
+    float *lse;
+    uint32_t *flags;
+};
+qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s);
 
 }  // namespace qsa

@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "qsa_device.cuh"
+#include "tc_ptx.cuh"
 #include "warp_topk.cuh"
 #include "qsa_internal.h"
 
@@ -42,7 +43,6 @@ constexpr int kEpiParts = 4;                  // epilogue warps per TMEM lane qu
 constexpr int kEpi = 128 * kEpiParts;         // epilogue threads
 constexpr int kThreads = 64 + kEpi;           // + one TMA warp and one MMA warp
 constexpr int kMaxChunks = (16 + kEpiParts - 1) / kEpiParts;  // 16-column chunks per thread
-constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s bound on any wait
 
 template <bool F32>
 struct Cfg;
@@ -113,127 +113,6 @@ struct KParams {
     int sb_stride;     // scores per query in the on-chip buffer (tiles_per_cta * 128)
 };
 
-// ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long now_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// One try_wait that may suspend the thread (up to ~65 us, or until the phase
-// completes), so waiting warps take no issue slots from working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(65536u)
-        : "memory");
-    return ok != 0;
-}
-// Wait for the phase of parity `parity` to complete.  Gives up when another
-// thread has aborted or after kWaitNs (then raises the abort itself).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (now_ns() - t0 > kWaitNs) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-// Bounded wait that never raises the abort (used while draining).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    const unsigned long long t0 = now_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (now_ns() - t0 > kWaitNs) return;
-}
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-template <bool F32>
-__device__ __forceinline__ void mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (F32) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-            : "memory");
-    }
-}
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// Ties loaded registers to a point after tcgen05.wait::ld, so that no use of
-// them is scheduled before the wait.
-__device__ __forceinline__ void reg_fence(uint32_t (&v)[16]) {
-    asm volatile(""
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
-                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
-                   "+r"(v[15]));
-}
-
 // sum_h w[h] * relu(acc[h]) for one query, in fp32: ReLU per head, then the
 // products added in two interleaved partial sums (packed two-wide FMA) that
 // are combined at the end.
@@ -272,24 +151,6 @@ __device__ __forceinline__ float head_sum(const float *w, const uint32_t *acc) {
     }
 }
 
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (SBO); the leading offset is unused for this layout.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-// Instruction descriptor: fp32 accumulator, A/B format `fmt`, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc(uint32_t fmt, int M, int N) {
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 
 // a = hi + lo with hi = a truncated to tf32 (exact split), in place for hi.
 __device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes, int tid, int nthreads) {
@@ -693,71 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-struct MapKey {
-    const void *ptr;
-    uint64_t rows;
-    uint32_t box_rows;
-    int f32;
-    int dev;
-    bool operator==(const MapKey &o) const {
-        return ptr == o.ptr && rows == o.rows && box_rows == o.box_rows && f32 == o.f32 && dev == o.dev;
-    }
-};
-
-// Small cache of encoded tensor maps (a map is 128 bytes of host data).
-qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint64_t rows, uint32_t box_rows) {
-    static std::mutex mu;
-    static MapKey keys[32];
-    static CUtensorMap maps[32];
-    static int used = 0, next = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const MapKey key{ptr, rows, box_rows, f32 ? 1 : 0, dev};
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        for (int i = 0; i < used; ++i)
-            if (keys[i] == key) {
-                *out = maps[i];
-                return QSA_OK;
-            }
-    }
-    auto fn = encode_fn();
-    if (!fn) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t dims[2] = {(cuuint64_t)QSA_HEAD_DIM, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)QSA_HEAD_DIM * (f32 ? 4 : 2)};
-    const cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUtensorMap m;
-    const CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        keys[next] = key;
-        maps[next] = m;
-        next = (next + 1) % 32;
-        if (used < 32) ++used;
-    }
-    *out = m;
-    return QSA_OK;
-}
-
 template <bool F32, int H, bool FUSED>
 qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
                         cudaStream_t s) {
@@ -839,9 +635,9 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     while (tmem_cols < 2 * bn) tmem_cols *= 2;
 
     CUtensorMap mk, mq;
-    qsa_status st = get_map(&mk, a.kblk, f32, (uint64_t)a.max_blocks, kBM);
+    qsa_status st = get_map(&mk, a.kblk, f32, QSA_HEAD_DIM, (uint64_t)a.max_blocks, kBM);
     if (st != QSA_OK) return st;
-    st = get_map(&mq, a.q, f32, (uint64_t)a.nq * H, (uint32_t)bn);
+    st = get_map(&mq, a.q, f32, QSA_HEAD_DIM, (uint64_t)a.nq * H, (uint32_t)bn);
     if (st != QSA_OK) return st;
 
     KParams kp{};

@@ -1,0 +1,468 @@
+// sel_attn.cu -- selection attention, forward, over the blocks each query selected.
+//
+//   o[q][h][:] = sum_t p_t V[g][t][:] / sum_t p_t,  p_t = exp(scale * (s_t - m)),
+//   s_t = dot(qa[q][h][:], K[g][t][:]),  m = max_t s_t,  g = h / 16,
+//
+// over the tokens t of the distinct selected blocks ids[q][*] (64 tokens each)
+// that lie below n_tokens[q].  This is the consumer of the block selection set
+// out in "[wave] NSA: LDS optimization for block-gather in selection attention"
+// (section "Problem": a query reads the tokens of its selected blocks, which are
+// scattered in memory; strategy 1: each block's K and V are staged on chip once
+// and read there by every head of the GQA group).
+//
+// One CTA per (query, KV head); the 16 heads of the group are the N side of
+// every MMA.  Two passes over on-chip data keep the softmax exact without
+// rescaling:
+//   1. S^T = K_pair . Q^T on tcgen05 (M = 128 tokens of two blocks, N = 16
+//      heads, K = 128), one TMEM tile per pair of blocks; all of a query's
+//      logits stay in TMEM (k <= 64 blocks -> at most 512 columns).
+//   2. Four softmax warps (one TMEM lane = one token each) take the per-head
+//      maximum over every visible token, then write p = exp2((s - m) * scale *
+//      log2 e) rounded to bf16 into a shared-memory ring and sum the rounded
+//      values, so the output is an exact convex combination of the weights used.
+//   3. O^T += V_b^T . P_b^T on tcgen05 (M = 128 head dims, N = 16 heads, K = 64
+//      tokens per block) accumulates in TMEM over the columns of the first
+//      logit tile, which is consumed first.
+// The V cache holds every 64-token block dimension-major ([128][64]), so both
+// operands of both products are K-major under the 128-byte swizzle that TMA
+// writes.  Warp 0 issues TMA loads (K pairs, then V pairs, through one ring),
+// warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax and the
+// epilogue.  Every wait is bounded; on expiry the CTA raises
+// QSA_FLAG_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "qsa_device.cuh"
+#include "tc_ptx.cuh"
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kG = 16;                  // heads per GQA group (MMA N)
+constexpr int kMaxSel = 64;             // blocks per query
+constexpr int kStages = 3;              // K/V ring stages
+constexpr int kStageBytes = 32768;      // two blocks of K (two 64-column halves) or of V^T
+constexpr int kPStages = 2;             // P ring stages
+constexpr int kPBytes = 4096;           // two blocks x 16 heads x 64 tokens bf16
+constexpr int kThreads = 192;           // TMA warp, MMA warp, four softmax warps
+constexpr int kSoft = 128;
+constexpr uint32_t kFmtBF16 = 1;
+
+constexpr int kOffQ = 0;                                  // 2 halves x 16 rows x 128 B
+constexpr int kOffKV = 4096;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;
+constexpr int kOffCtrl = kOffP + kPStages * kPBytes;
+
+struct AttnCtrl {
+    uint64_t qfull;
+    uint64_t full[kStages], empty[kStages];
+    uint64_t sfull;                      // every logit tile written
+    uint64_t pfull[kPStages], pempty[kPStages];
+    uint64_t tailbar;                    // the V block holding the end of the context landed
+    uint64_t ofull;                      // the output accumulator complete
+    uint64_t done;                       // every MMA complete (teardown)
+    uint32_t tmem_base;
+    int abort;
+    int nsel;
+    int ntok;
+    int32_t raw[kMaxSel];
+    int32_t sel[kMaxSel];                // the distinct valid ids, in slot order
+    float red[4][kG];
+    float m[kG];                         // per-head maximum logit (unscaled)
+    float l[kG];                         // per-head sum of the rounded weights
+};
+constexpr int kSmemBytes = kOffCtrl + (int)sizeof(AttnCtrl) + 1024;   // + alignment slack
+// more than half of an SM's shared memory: one CTA per SM, for queries whose
+// logits take all 512 TMEM columns
+constexpr int kSmemOneBytes = 120 * 1024;
+static_assert(kSmemBytes <= kSmemOneBytes, "attention shared memory");
+
+struct AttnParams {
+    const int32_t *ids;
+    const int32_t *n_tokens;
+    float *out;
+    float *lse;
+    uint32_t *flags;
+    int n_heads, n_kv, k, capacity, nb_cap;
+    float scale, scale_log2;
+};
+
+__device__ __forceinline__ void soft_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Every lane of the calling warp learns whether lane 0's bounded wait succeeded.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
+
+// Byte offset of (row, col) of a bf16 tile with 128-byte rows under the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    return (uint32_t)(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2);
+}
+
+// Zero tokens r..63 of a 64-token V^T block ([128 dims][64 tokens], swizzled), one
+// warp.
+__device__ __forceinline__ void clear_tail(uint8_t *blk, int r) {
+    const int lane = threadIdx.x & 31;
+    for (int d = lane; d < 128; d += 32)
+        for (int c = r >> 3; c < 8; ++c) {
+            uint8_t *chunk = blk + swz(d, 8 * c);
+            if (8 * c >= r) {
+                *reinterpret_cast<uint4 *>(chunk) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                uint16_t *e = reinterpret_cast<uint16_t *>(chunk);
+                for (int t = r - 8 * c; t < 8; ++t) e[t] = 0;
+            }
+        }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sel_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sQ = smem + kOffQ;
+    uint8_t *sKV = smem + kOffKV;
+    uint8_t *sP = smem + kOffP;
+    AttnCtrl &ct = *reinterpret_cast<AttnCtrl *>(smem + kOffCtrl);
+    volatile int *abort_flag = &ct.abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qi = blockIdx.x / p.n_kv, g = blockIdx.x % p.n_kv;
+    const int head0 = g * kG;
+
+    if (tid == 32) {
+        mbar_init(&ct.qfull, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ct.full[s], 2);   // the producer's expect-tx arrival and its release arrival
+            mbar_init(&ct.empty[s], 1);
+        }
+        mbar_init(&ct.tailbar, 1);
+        mbar_init(&ct.sfull, 1);
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&ct.pfull[s], kSoft);
+            mbar_init(&ct.pempty[s], 1);
+        }
+        mbar_init(&ct.ofull, 1);
+        mbar_init(&ct.done, 1);
+        ct.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {   // the group's 16 query rows, two 64-column halves
+        mbar_expect_tx(&ct.qfull, 2 * kG * 128);
+        for (int hh = 0; hh < 2; ++hh)
+            tma_load_2d(sQ + hh * kG * 128, &tm_q, &ct.qfull, hh * 64, qi * p.n_heads + head0);
+    }
+    if (warp == 2) {
+        // the query's distinct ids inside its context, in slot order
+        int ntok = p.n_tokens[qi];
+        if (ntok < 0 || ntok > p.capacity) {
+            if (lane == 0 && g == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
+            ntok = ntok < 0 ? 0 : p.capacity;
+        }
+        const int nb = (ntok + 63) >> 6;
+        for (int j = lane; j < p.k; j += 32) ct.raw[j] = p.ids[(size_t)qi * p.k + j];
+        __syncwarp();
+        int cnt = 0;
+        bool bad = false;
+        for (int j0 = 0; j0 < p.k; j0 += 32) {
+            const int j = j0 + lane;
+            const int32_t b = j < p.k ? ct.raw[j] : -1;
+            bool take = b >= 0 && b < nb;
+            bad |= j < p.k && b != -1 && !take;
+            for (int i = 0; take && i < j; ++i) take = ct.raw[i] != b;
+            const unsigned m = __ballot_sync(kFull, take);
+            if (take) ct.sel[cnt + __popc(m & ((1u << lane) - 1u))] = b;
+            cnt += __popc(m);
+        }
+        if (__any_sync(kFull, bad) && lane == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_BAD_ID);
+        if (lane == 0) {
+            ct.nsel = cnt;
+            ct.ntok = ntok;
+        }
+    }
+    __syncthreads();
+    const int nsel = ct.nsel, ntok = ct.ntok;
+    const int T = (nsel + 1) >> 1;   // pair tiles
+    float *out = p.out + ((size_t)qi * p.n_heads + head0) * 128;
+    if (nsel == 0) {   // no visible token: o = 0, lse = -inf
+        if (warp >= 2) {
+            for (int i = tid - 64; i < kG * 128; i += kSoft) out[i] = 0.0f;
+            if (p.lse && tid - 64 < kG) p.lse[(size_t)qi * p.n_heads + head0 + tid - 64] = -INFINITY;
+        }
+        if (tid == 0) mbar_drain(&ct.qfull, 0);
+        return;
+    }
+    uint32_t ncols = 32;
+    while ((int)ncols < T * 16) ncols <<= 1;
+    if (warp == 1) {
+        tmem_alloc(&ct.tmem_base, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ct.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- producer: K pairs 0..T-1, then V pairs 0..T-1.  Lane 0
+        // issues; the whole warp clears the V tokens past the context of the block
+        // that holds its end, after that block lands and before the stage is
+        // released to the MMA (its weights are 0, but 0 x NaN would not be).
+        int issued = 0;
+        bool tail_issued = false;
+        for (int i = 0; i < 2 * T; ++i) {
+            const int s = i % kStages;
+            if (!warp_wait(&ct.empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort_flag)) break;
+            const int tile = i < T ? i : i - T;
+            const int nb_t = min(2, nsel - 2 * tile);
+            uint8_t *st = sKV + s * kStageBytes;
+            int tail_j = -1;
+            if (i >= T)
+                for (int j = 0; j < nb_t; ++j)
+                    if ((ct.sel[2 * tile + j] + 1) * 64 > ntok) tail_j = j;
+            if (lane == 0) {
+                mbar_expect_tx(&ct.full[s], (uint32_t)((nb_t - (tail_j >= 0 ? 1 : 0)) * 16384));   // arrival 1
+                if (tail_j >= 0) mbar_expect_tx(&ct.tailbar, 16384u);
+                for (int j = 0; j < nb_t; ++j) {
+                    const int b = ct.sel[2 * tile + j];
+                    if (i < T) {   // 64 token rows, two 64-column halves of 16 KB regions
+                        const int y = g * p.capacity + b * 64;
+                        tma_load_2d(st + j * 8192, &tm_k, &ct.full[s], 0, y);
+                        tma_load_2d(st + 16384 + j * 8192, &tm_k, &ct.full[s], 64, y);
+                    } else {       // 128 dimension rows of 64 tokens
+                        tma_load_2d(st + j * 16384, &tm_v, j == tail_j ? &ct.tailbar : &ct.full[s], 0,
+                                    (g * p.nb_cap + b) * 128);
+                    }
+                }
+            }
+            if (tail_j >= 0) {   // at most one block per query holds the end of its context
+                tail_issued = true;
+                if (warp_wait(&ct.tailbar, 0, abort_flag))
+                    clear_tail(st + tail_j * 16384, ntok - ct.sel[2 * tile + tail_j] * 64);
+                fence_proxy_async();
+                __syncwarp();
+            }
+            if (lane == 0) mbar_arrive(&ct.full[s]);   // arrival 2
+            ++issued;
+        }
+        if (lane == 0) {
+            for (int j = max(0, issued - kStages); j < issued; ++j)
+                mbar_drain(&ct.full[j % kStages], (uint32_t)(j / kStages) & 1u);
+            if (tail_issued) mbar_drain(&ct.tailbar, 0);
+            mbar_drain(&ct.qfull, 0);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t id = idesc(kFmtBF16, 128, kG);
+            bool ok = mbar_wait(&ct.qfull, 0, abort_flag);
+            tc_fence_after();
+            const uint32_t q0 = smem_u32(sQ);
+            for (int i = 0; ok && i < T; ++i) {   // logits of pair i -> columns 16 i
+                const int s = i % kStages;
+                if (!(ok = mbar_wait(&ct.full[s], (uint32_t)(i / kStages) & 1u, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sKV + s * kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma<false>(tmem + (uint32_t)(i * 16), sdesc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                               sdesc(q0 + (kk >> 2) * (kG * 128) + (kk & 3) * 32), id, kk > 0 ? 1u : 0u);
+                mma_commit(&ct.empty[s]);
+            }
+            if (ok) mma_commit(&ct.sfull);
+            for (int i = 0; ok && i < T; ++i) {   // output: columns 0..15, after pair 0 is consumed
+                const int r = T + i, s = r % kStages, ps = i % kPStages;
+                if (!(ok = mbar_wait(&ct.full[s], (uint32_t)(r / kStages) & 1u, abort_flag))) break;
+                if (!(ok = mbar_wait(&ct.pfull[ps], (uint32_t)(i / kPStages) & 1u, abort_flag))) break;
+                tc_fence_after();
+                const int nb_t = min(2, nsel - 2 * i);
+                const uint32_t a0 = smem_u32(sKV + s * kStageBytes), b0 = smem_u32(sP + ps * kPBytes);
+                for (int j = 0; j < nb_t; ++j)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma<false>(tmem, sdesc(a0 + j * 16384 + kk * 32), sdesc(b0 + j * 2048 + kk * 32), id,
+                                   (i | j | kk) != 0 ? 1u : 0u);
+                mma_commit(&ct.empty[s]);
+                mma_commit(&ct.pempty[ps]);
+            }
+            if (ok) mma_commit(&ct.ofull);
+            mma_commit(&ct.done);
+            mbar_drain(&ct.done, 0);
+        }
+    } else {
+        // ---------------- softmax and epilogue: one TMEM lane (a token of a pair,
+        // later a head dimension) per thread.  Every thread reaches every named
+        // barrier, whatever the waits returned.
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int half = row >> 6, tok = row & 63;
+        const int sw = warp - 2;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        auto visible = [&](int i) {
+            const int j = 2 * i + half;
+            return j < nsel && ct.sel[j] * 64 + tok < ntok;
+        };
+        bool ok = warp_wait(&ct.sfull, 0, abort_flag);
+        tc_fence_after();
+        float mx[kG];
+#pragma unroll
+        for (int h = 0; h < kG; ++h) mx[h] = -INFINITY;
+        if (ok) {
+            for (int i0 = 0; i0 < T; i0 += 4) {
+                uint32_t v[4][16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (i0 + u < T) tmem_ld16_nowait(lane_addr + (uint32_t)((i0 + u) * 16), v[u]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    reg_fence(v[u]);
+                    if (i0 + u < T && visible(i0 + u))
+#pragma unroll
+                        for (int h = 0; h < kG; ++h) mx[h] = fmaxf(mx[h], __uint_as_float(v[u][h]));
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int h = 0; h < kG; ++h) ct.red[sw][h] = mx[h];
+        soft_barrier();
+        float mc[kG];   // m * scale * log2(e)
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+            const float m = fmaxf(fmaxf(ct.red[0][h], ct.red[1][h]), fmaxf(ct.red[2][h], ct.red[3][h]));
+            mc[h] = m * p.scale_log2;
+            if (row == 0) ct.m[h] = m;
+        }
+        float l[kG];
+#pragma unroll
+        for (int h = 0; h < kG; ++h) l[h] = 0.0f;
+        for (int i = 0; ok && i < T; ++i) {
+            const int ps = i % kPStages;
+            if (i >= kPStages && !(ok = warp_wait(&ct.pempty[ps], (uint32_t)((i / kPStages) - 1) & 1u, abort_flag)))
+                break;
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16_nowait(lane_addr + (uint32_t)(i * 16), v);
+            tmem_wait_ld();
+            reg_fence(v);
+            if (2 * i + half < nsel) {   // this row's block exists: write its weights (0 past the context)
+                const bool vis = visible(i);
+                uint8_t *pb = sP + ps * kPBytes + half * 2048;
+#pragma unroll
+                for (int h = 0; h < kG; ++h) {
+                    const float e = vis ? exp2f(fmaf(__uint_as_float(v[h]), p.scale_log2, -mc[h])) : 0.0f;
+                    const __nv_bfloat16 eb = __float2bfloat16_rn(e);
+                    l[h] += __bfloat162float(eb);
+                    *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, tok)) = eb;
+                }
+            }
+            fence_proxy_async();   // the weights are read by the tensor core
+            tc_fence_before();
+            mbar_arrive(&ct.pfull[ps]);
+        }
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l[h] += __shfl_xor_sync(kFull, l[h], o);
+        }
+        soft_barrier();   // every warp has read ct.red
+        if (lane == 0)
+#pragma unroll
+            for (int h = 0; h < kG; ++h) ct.red[sw][h] = l[h];
+        soft_barrier();
+        if (row < kG) ct.l[row] = (ct.red[0][row] + ct.red[1][row]) + (ct.red[2][row] + ct.red[3][row]);
+        soft_barrier();
+        ok = ok && warp_wait(&ct.ofull, 0, abort_flag);
+        tc_fence_after();
+        if (ok) {
+            uint32_t o[16];
+            tmem_ld16_nowait(lane_addr, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            // row = head dimension d; a warp's stores for one head are 32 consecutive floats
+#pragma unroll
+            for (int h = 0; h < kG; ++h) out[h * 128 + row] = __uint_as_float(o[h]) / ct.l[h];
+            if (p.lse && row < kG)
+                p.lse[(size_t)qi * p.n_heads + head0 + row] = p.scale * ct.m[row] + logf(ct.l[row]);
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+    if (tid == 0 && ct.abort && p.flags) atomicOr(p.flags, QSA_FLAG_WAIT_TIMEOUT);
+}
+
+template <int Bytes>
+qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &ap,
+                       int grid, cudaStream_t s) {
+    static std::mutex mu;
+    static bool opted_in[64] = {false};
+    int dev = 0;
+    qsa_status st = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != QSA_OK) return st;
+    if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!opted_in[dev]) {
+            st = check_cuda(cudaFuncSetAttribute(sel_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemOneBytes),
+                            "cudaFuncSetAttribute(selection attention)");
+            if (st != QSA_OK) return st;
+            opted_in[dev] = true;
+        }
+    }
+    sel_attn_kernel<<<grid, kThreads, Bytes, s>>>(mq, mk, mv, ap);
+    return check_cuda(cudaGetLastError(), "sel_attn_kernel launch");
+}
+
+}  // namespace
+
+qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s) {
+    CUtensorMap mq, mk, mv;
+    qsa_status st = get_map(&mq, a.qa, false, QSA_HEAD_DIM, (uint64_t)a.nq * a.n_heads, kG);
+    if (st != QSA_OK) return st;
+    st = get_map(&mk, a.kcache, false, QSA_HEAD_DIM, (uint64_t)a.n_kv_heads * a.capacity, 64);
+    if (st != QSA_OK) return st;
+    st = get_map(&mv, a.vcache_t, false, 64, (uint64_t)a.n_kv_heads * a.capacity * 2, 128);
+    if (st != QSA_OK) return st;
+    AttnParams ap{};
+    ap.ids = a.ids;
+    ap.n_tokens = a.n_tokens;
+    ap.out = a.out;
+    ap.lse = a.lse;
+    ap.flags = a.flags;
+    ap.n_heads = a.n_heads;
+    ap.n_kv = a.n_kv_heads;
+    ap.k = a.k;
+    ap.capacity = a.capacity;
+    ap.nb_cap = a.capacity / 64;
+    ap.scale = a.scale;
+    ap.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+    const int grid = a.nq * a.n_kv_heads;
+    // k > 32 blocks can take all 512 TMEM columns: one CTA per SM
+    return a.k > 32 ? launch_with<kSmemOneBytes>(mq, mk, mv, ap, grid, s)
+                    : launch_with<kSmemBytes>(mq, mk, mv, ap, grid, s);
+}
+
+}  // namespace qsa

@@ -40,10 +40,15 @@ def blocks_for_tokens(tokens):
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """fp32 -> bf16 bit patterns (uint16), round to nearest even (inputs are finite)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return rounded.astype(np.uint16)
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even (inputs are finite:
+    the largest finite pattern plus the rounding increment stays below 2^32)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).reshape(-1)
+    out = np.empty(u.shape, dtype=np.uint16)
+    step = 1 << 24
+    for i in range(0, u.size, step):   # bounded temporaries on large caches
+        c = u[i:i + step]
+        out[i:i + step] = (c + np.uint32(0x7FFF) + ((c >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return out.reshape(np.shape(x))
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -225,6 +230,27 @@ def random_ids(seed: int, n_blocks, k: int, n_valid=None) -> np.ndarray:
     return out
 
 
+def normal_bf16(seed: int, shape, chunks: int = 16) -> np.ndarray:
+    """N(0,1) draws rounded to bf16 bits, in ``chunks`` equal slices of the flat array,
+    slice i from the i-th PCG64 stream spawned from ``seed`` (filled in parallel
+    threads; the values do not depend on the thread count)."""
+    import concurrent.futures as cf
+    import os
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    streams = np.random.SeedSequence(seed).spawn(chunks)
+    bounds = [(i * n // chunks, (i + 1) * n // chunks) for i in range(chunks)]
+
+    def fill(i):
+        lo, hi = bounds[i]
+        g = np.random.Generator(np.random.PCG64(streams[i]))
+        out[lo:hi] = to_bf16_bits(g.standard_normal(hi - lo, dtype=np.float32))
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(chunks, os.cpu_count() or 1))) as ex:
+        list(ex.map(fill, range(chunks)))
+    return out.reshape(shape)
+
+
 def make_attention_case(seed: int, nq: int, n_kv_heads: int, capacity_tokens: int, tokens, k: int, *,
                         group: int = 16, ids: np.ndarray | None = None, n_valid=None,
                         name: str = "") -> AttnCase:
@@ -233,13 +259,33 @@ def make_attention_case(seed: int, nq: int, n_kv_heads: int, capacity_tokens: in
     rng = np.random.default_rng(seed)
     H = n_kv_heads * group
     qa = to_bf16_bits(rng.standard_normal((nq, H, HEAD_DIM), dtype=np.float32))
-    kc = to_bf16_bits(rng.standard_normal((n_kv_heads, capacity_tokens, HEAD_DIM), dtype=np.float32))
-    vc = to_bf16_bits(rng.standard_normal((n_kv_heads, capacity_tokens, HEAD_DIM), dtype=np.float32))
+    kc = normal_bf16(seed + 2, (n_kv_heads, capacity_tokens, HEAD_DIM))
+    vc = normal_bf16(seed + 3, (n_kv_heads, capacity_tokens, HEAD_DIM))
     toks = np.broadcast_to(np.asarray(tokens, dtype=np.int64), (nq,)).astype(np.int32)
     if ids is None:
         ids = random_ids(seed + 1, blocks_for_tokens(toks), k, n_valid)
     return AttnCase(qa=qa, kc=kc, vc=vc, ids=np.ascontiguousarray(ids, dtype=np.int32), n_tokens=toks,
                     scale=HEAD_DIM ** -0.5, name=name)
+
+
+ATTN_KV_HEADS = 4
+
+
+def deep_attention_case(ids: np.ndarray | None = None) -> AttnCase:
+    """Selection attention at the deep prompt's depth: 256 queries x 64 heads (4 GQA
+    groups of 16), bf16, capacity 524,288 tokens, contexts of 520,000 tokens, k = 32
+    (random distinct blocks of the context unless ``ids`` are given)."""
+    return make_attention_case(4100, 256, ATTN_KV_HEADS, 524_288, 520_000, 32, ids=ids,
+                               name="deep prompt attention: 256q x 64 heads (4 groups of 16) bf16, "
+                                    "520,000 tokens, capacity 524,288, k = 32")
+
+
+def decode_attention_case(ids: np.ndarray | None = None) -> AttnCase:
+    """Selection attention for a decode window: 3 queries x 64 heads (4 GQA groups of
+    16), bf16, capacity 262,144 tokens, contexts of 258,000 tokens, k = 32."""
+    return make_attention_case(2100, 3, ATTN_KV_HEADS, 262_144, 258_000, 32, ids=ids,
+                               name="decode attention: 3q x 64 heads (4 groups of 16) bf16, "
+                                    "258,000 tokens, capacity 262,144, k = 32")
 
 
 def vcache_blocks_transposed(vc: np.ndarray) -> np.ndarray:

@@ -26,12 +26,15 @@ PATH_NAMES = {PATH_AUTO: "auto", PATH_SPLIT: "split", PATH_SAMPLE: "sample",
               PATH_REGISTER: "register", PATH_RADIX: "radix", PATH_WARP: "warp"}
 # flags word bits
 FLAG_NBLOCKS_CLAMPED, FLAG_WAIT_TIMEOUT, FLAG_INTERNAL, FLAG_SAMPLE_FALLBACK = 0x1, 0x2, 0x4, 0x8
-ERROR_FLAGS = FLAG_NBLOCKS_CLAMPED | FLAG_WAIT_TIMEOUT | FLAG_INTERNAL
+FLAG_BAD_ID = 0x10
+ERROR_FLAGS = FLAG_NBLOCKS_CLAMPED | FLAG_WAIT_TIMEOUT | FLAG_INTERNAL | FLAG_BAD_ID
 HEAD_DIM = 128
 MAX_K = 1024
+ATTN_GROUP = 16
+ATTN_MAX_K = 64
 
 EXPORTS = ("qsa_workspace_bytes", "qsa_workspace_init", "qsa_block_scores", "qsa_block_topk",
-           "qsa_block_topk_static", "qsa_select", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
+           "qsa_block_topk_static", "qsa_select", "qsa_select_attention", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
            "qsa_version")
 
 
@@ -68,6 +71,9 @@ def load() -> ctypes.CDLL:
     lib.qsa_select.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i64, i32, vp,
                                sz, i32, vp]
     lib.qsa_select.restype = i32
+    lib.qsa_select_attention.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                                         ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.qsa_select_attention.restype = i32
     lib.qsa_read_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.qsa_read_flags.restype = i32
     lib.qsa_auto_path.argtypes = [i32, i32, i32, i32]
@@ -209,6 +215,39 @@ def select(q: torch.Tensor, w: torch.Tensor, kblk: torch.Tensor, n_blocks: torch
                         int(bool(fused)), _dptr(ws, "ws"), ws.numel(), path, _stream(stream))
     _check("qsa_select", st)
     return ids
+
+
+def select_attention(qa: torch.Tensor, kcache: torch.Tensor, vcache_t: torch.Tensor, ids: torch.Tensor,
+                     n_tokens: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None = None,
+                     scale: float | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Selection attention over ids [nq, k]: out [nq, H, 128] fp32 (and lse [nq, H]).
+
+    qa [nq, H, 128] bf16, kcache [Hkv, C, 128] bf16, vcache_t [Hkv, C/64, 128, 64] bf16
+    (each block of V dimension-major), n_tokens [nq] int32; H = 16 * Hkv."""
+    lib = load()
+    for t, nm in ((qa, "qa"), (kcache, "kcache"), (vcache_t, "vcache_t"), (ids, "ids"), (n_tokens, "n_tokens"),
+                  (out, "out")):
+        _contig(t, nm)
+    if qa.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16 or vcache_t.dtype != torch.bfloat16:
+        raise ValueError("qa, kcache and vcache_t must be bfloat16")
+    if ids.dtype != torch.int32 or n_tokens.dtype != torch.int32:
+        raise ValueError("ids and n_tokens must be int32")
+    nq, H, D = qa.shape
+    Hkv, C, _ = kcache.shape
+    if tuple(vcache_t.shape) != (Hkv, C // 64, D, 64):
+        raise ValueError("vcache_t must be [n_kv_heads, capacity / 64, 128, 64]")
+    if out.dtype != torch.float32 or tuple(out.shape) != (nq, H, D):
+        raise ValueError("out must be a contiguous fp32 tensor [nq, n_heads, 128]")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (nq, H) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 tensor [nq, n_heads]")
+    if scale is None:
+        scale = D ** -0.5
+    st = lib.qsa_select_attention(_dptr(qa, "qa"), _dptr(kcache, "kcache"), _dptr(vcache_t, "vcache_t"), BF16,
+                                  _dptr(ids, "ids"), ids.shape[1], _dptr(n_tokens, "n_tokens"), nq, H, Hkv, D, C,
+                                  float(scale), _dptr(out, "out"), _dptr(lse, "lse"), _dptr(ws, "ws"),
+                                  0 if ws is None else ws.numel(), _stream(stream))
+    _check("qsa_select_attention", st)
+    return out
 
 
 def read_flags(ws: torch.Tensor, clear: bool = True, stream=None) -> int:

@@ -11,6 +11,14 @@ Rule (c): the end-to-end ids equal the oracle's FP64 selection, except for a
           is below tol; such a query is counted and must still be a valid
           tolerance top-k (every selected ref >= s_(k) - tol*scale, every other
           ref <= s_(k) + tol*scale).  Exact FP64 ties (gap 0) are not excused.
+Rule (d), selection attention: per (query, head, dim),
+          |o_gpu - o_ref| <= (2^-8 + 2^-12) * sum_t w_t |v_t| + 1e-7, and
+          |lse_gpu - lse_ref| <= 2^-9 + 1e-5 (1 + |lse_ref|).  The GPU rounds each
+          weight to bf16 (relative error <= 2^-9) and divides by the sum of the
+          rounded weights, so every normalised weight is within 2^-8 (1 + 2^-9)
+          of the exact one; 2^-12 covers the fp32 accumulation.  sum_t w_t |v_t|
+          is the oracle's output on |V|.  An empty token set gives exactly 0 and
+          -inf.
 """
 from __future__ import annotations
 
@@ -100,3 +108,49 @@ def check_rule_c(gpu_ids, ref_scores, ref_ids, n_blocks, k, dtype, tight_tol=Non
     r = rule_c(gpu_ids, ref_scores, ref_ids, n_blocks, k, TOL[dtype], tight_tol)
     assert r["failed"] == 0, f"rule (c): {r['failed']} queries fail, first {r['failed_ids'][:5]}"
     return r
+
+
+ATTN_REL = 2.0 ** -8 + 2.0 ** -12
+
+
+def attn_to_device(case, device="cuda"):
+    """(qa, kcache, vcache_t, ids, n_tokens) of an AttnCase on the device."""
+    import torch
+    from sparse_attention_kv_gb300 import inputs
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return (bf(case.qa), bf(case.kc), bf(inputs.vcache_blocks_transposed(case.vc)),
+            torch.from_numpy(case.ids).to(device), torch.from_numpy(case.n_tokens).to(device))
+
+
+def attention_reference(case, rows=None):
+    """Oracle (out, lse, sum_t w_t |v_t|) for the queries ``rows`` (all by default)."""
+    import oracle
+    r = slice(None) if rows is None else np.asarray(rows)
+    qa, ids, nt = case.qa[r], case.ids[r], case.n_tokens[r]
+    out, lse = oracle.select_attention(qa, case.kc, case.vc, ids, nt, case.scale)
+    wabs, _ = oracle.select_attention(qa, case.kc, case.vc & np.uint16(0x7FFF), ids, nt, case.scale)
+    return out, lse, wabs
+
+
+def check_rule_d(out_gpu, lse_gpu, out_ref, lse_ref, wabs):
+    """Assert rule (d); returns the largest error as a fraction of its bound."""
+    out_gpu = np.asarray(out_gpu, np.float64)
+    empty = np.isneginf(lse_ref)
+    assert (out_gpu[empty] == 0).all(), "an empty token set gave a nonzero output"
+    if lse_gpu is not None:
+        assert np.isneginf(np.asarray(lse_gpu)[empty]).all(), "an empty token set gave a finite lse"
+    full = ~empty
+    bound = ATTN_REL * wabs[full] + 1e-7
+    err = np.abs(out_gpu[full] - out_ref[full])
+    assert np.isfinite(out_gpu[full]).all(), "non-finite output"
+    worst = float((err / bound).max()) if err.size else 0.0
+    assert worst <= 1.0, f"rule (d): output error {worst:.3f} x its bound"
+    if lse_gpu is not None and full.any():
+        lg = np.asarray(lse_gpu, np.float64)[full]
+        lb = 2.0 ** -9 + 1e-5 * (1 + np.abs(lse_ref[full]))
+        le = np.abs(lg - lse_ref[full])
+        assert (le <= lb).all(), f"rule (d): lse error {float((le / lb).max()):.3f} x its bound"
+        worst = max(worst, float((le / lb).max()))
+    return worst

@@ -98,6 +98,37 @@ def test_select_rejects_bad_arguments_before_launch(lib, case, status):
     assert lib.qsa_last_error().decode()
 
 
+@pytest.mark.parametrize("case,status", [
+    (dict(qa=None), qsa.ERR_INVALID_ARG),
+    (dict(out=None), qsa.ERR_INVALID_ARG),
+    (dict(nq=0), qsa.ERR_INVALID_ARG),
+    (dict(head_dim=64), qsa.ERR_INVALID_ARG),
+    (dict(n_heads=32), qsa.ERR_INVALID_ARG),      # not 16 x n_kv_heads
+    (dict(n_kv=0, n_heads=0), qsa.ERR_INVALID_ARG),
+    (dict(k=0), qsa.ERR_INVALID_ARG),
+    (dict(k=65), qsa.ERR_INVALID_ARG),
+    (dict(capacity=100), qsa.ERR_INVALID_ARG),
+    (dict(capacity=0), qsa.ERR_INVALID_ARG),
+    (dict(capacity=1 << 29, n_kv=2, n_heads=32), qsa.ERR_INVALID_ARG),
+    (dict(kcache=FAKE + 8), qsa.ERR_INVALID_ARG),
+    (dict(scale=0.0), qsa.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), qsa.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), qsa.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), qsa.ERR_WORKSPACE),
+    (dict(ws=FAKE + 64), qsa.ERR_WORKSPACE),
+    (dict(dt=qsa.F32), qsa.ERR_UNSUPPORTED),
+])
+def test_select_attention_rejects_bad_arguments_before_launch(lib, case, status):
+    a = dict(qa=FAKE, kcache=FAKE, vcache=FAKE, dt=qsa.BF16, ids=FAKE, k=32, n_tokens=FAKE, nq=4, n_heads=64,
+             n_kv=4, head_dim=128, capacity=4096, scale=128 ** -0.5, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=256)
+    a.update(case)
+    st = lib.qsa_select_attention(a["qa"], a["kcache"], a["vcache"], a["dt"], a["ids"], a["k"], a["n_tokens"],
+                                  a["nq"], a["n_heads"], a["n_kv"], a["head_dim"], a["capacity"], a["scale"],
+                                  a["out"], a["lse"], a["ws"], a["ws_bytes"], None)
+    assert st == status
+    assert lib.qsa_last_error().decode()
+
+
 def test_topk_rejects_bad_arguments_before_launch(lib):
     st = lib.qsa_block_topk(FAKE, 100, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 0, None)
     assert st == qsa.ERR_INVALID_ARG   # stride < max_blocks

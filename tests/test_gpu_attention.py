@@ -1,0 +1,184 @@
+"""Selection attention on the GPU against the FP64 oracle (parity rule (d)).
+
+Small cases span several pair tiles, odd block counts, pads, ragged contexts
+with partial tail blocks, k = 1 .. 64 (the one-CTA-per-SM form above 32),
+several GQA groups, unsorted and repeated ids, ids past the context, NaN in the
+cache rows past the context, empty token sets, and the ids the select path
+itself produces.  The bench's configuration (256 queries x 64 heads in 4 GQA
+groups, 520,000 tokens, k = 32) is checked on sampled queries.
+"""
+import numpy as np
+import pytest
+
+from sparse_attention_kv_gb300 import inputs
+
+from .parity import attn_to_device, attention_reference, check_rule_d, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from sparse_attention_kv_gb300 import qsa as q
+    q.load()
+    return q
+
+
+def _run(qsa, case, ws=None, lse=True, ids=None, n_tokens=None):
+    qa, kc, vt, d_ids, d_nt = attn_to_device(case)
+    if ids is not None:
+        d_ids = ids
+    if n_tokens is not None:
+        d_nt = n_tokens
+    out = torch.full((case.nq, case.n_heads, 128), float("nan"), device="cuda")
+    lse_t = torch.full((case.nq, case.n_heads), float("nan"), device="cuda") if lse else None
+    qsa.select_attention(qa, kc, vt, d_ids, d_nt, out, lse_t, scale=case.scale, ws=ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), (lse_t.cpu().numpy() if lse else None)
+
+
+def _ws(qsa):
+    return torch.zeros(256, dtype=torch.uint8, device="cuda")
+
+
+CASES = [
+    # (seed, nq, n_kv, capacity, tokens, k, n_valid)
+    (101, 1, 1, 4096, 4096, 32, None),
+    (102, 16, 2, 8192, "ragged", 32, None),
+    (103, 8, 1, 4096, 4000, 1, None),
+    (104, 8, 3, 4096, "ragged", 7, None),
+    (105, 6, 1, 8192, 8192, 64, None),
+    (106, 6, 2, 8192, "ragged", 33, None),
+    (107, 12, 1, 4096, 4096, 32, "random"),
+    (108, 5, 4, 2048, "ragged", 16, None),
+]
+
+
+def _case(seed, nq, n_kv, cap, tokens, k, n_valid):
+    if tokens == "ragged":
+        tokens = inputs.ragged_tokens(seed, nq, cap // 64)
+    if n_valid == "random":
+        n_valid = np.random.default_rng(seed).integers(0, k + 1, size=nq)
+    return inputs.make_attention_case(seed, nq, n_kv, cap, tokens, k, n_valid=n_valid)
+
+
+@pytest.mark.parametrize("params", CASES, ids=[f"nq{c[1]}-kv{c[2]}-C{c[3]}-{c[4]}-k{c[5]}" for c in CASES])
+def test_matches_oracle(qsa, params):
+    c = _case(*params)
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    ref, ref_lse, wabs = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, wabs)
+    assert qsa.read_flags(ws) == 0
+
+
+def test_without_lse_or_workspace_the_output_is_the_same(qsa):
+    c = _case(*CASES[1])
+    a, _ = _run(qsa, c, _ws(qsa))
+    b, _ = _run(qsa, c, None, lse=False)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_unsorted_repeated_and_out_of_context_ids(qsa):
+    c = _case(111, 8, 2, 4096, "ragged", 32, 24)
+    rng = np.random.default_rng(5)
+    ids = c.ids.copy()
+    nb = inputs.blocks_for_tokens(c.n_tokens)
+    for q in range(c.nq):
+        row = ids[q]
+        m = int((row >= 0).sum())
+        row[m:m + 3] = [row[0], nb[q] + 5, -7]     # a repeat, one past the context, a negative
+        ids[q] = rng.permutation(row)
+    c.ids = ids
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    ref, ref_lse, wabs = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, wabs)
+    assert qsa.read_flags(ws) == qsa.FLAG_BAD_ID
+
+
+def test_cache_rows_past_the_context_take_no_part(qsa):
+    """NaN in every K and V row at or past each query's context: outputs unchanged, bit for bit."""
+    n = 64 * 37 + 23                                   # a partial tail block
+    c = inputs.make_attention_case(112, 8, 1, 4096, n, 32)
+    base = inputs.random_ids(113, np.full(8, 37), 31)
+    for q in range(8):                                 # 31 blocks below the tail, then the tail block
+        v = base[q][base[q] >= 0]
+        c.ids[q] = np.r_[v, 37, np.full(31 - len(v), -1)]
+    clean, clean_lse = _run(qsa, c)
+    nan = np.uint16(0x7FC0)
+    c.kc = c.kc.copy()
+    c.vc = c.vc.copy()
+    c.kc[:, n:] = nan
+    c.vc[:, n:] = nan
+    dirty, dirty_lse = _run(qsa, c)
+    np.testing.assert_array_equal(dirty, clean)
+    np.testing.assert_array_equal(dirty_lse, clean_lse)
+    ref, ref_lse, wabs = attention_reference(c)
+    check_rule_d(dirty, dirty_lse, ref, ref_lse, wabs)
+
+
+def test_empty_token_sets(qsa):
+    c = _case(114, 4, 2, 2048, 2048, 8, None)
+    c.ids[0] = -1                     # pads only
+    c.n_tokens[1] = 0                 # no context (its ids are then out of context)
+    c.ids[2] = -1
+    c.ids[2, 0] = 31                  # in context
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    ref, ref_lse, wabs = attention_reference(c)
+    assert np.isneginf(ref_lse[:2]).all()
+    check_rule_d(out, lse, ref, ref_lse, wabs)
+    assert qsa.read_flags(ws) == qsa.FLAG_BAD_ID
+
+
+def test_context_past_capacity_is_clamped(qsa):
+    c = _case(115, 4, 1, 2048, 2048, 8, None)
+    c.n_tokens[2] = 10 ** 6
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    c.n_tokens[2] = 2048
+    ref, ref_lse, wabs = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, wabs)
+    assert qsa.read_flags(ws) == qsa.FLAG_NBLOCKS_CLAMPED
+
+
+def test_on_the_ids_of_the_select_path(qsa):
+    """Select (chained and fused) on a 131,072-token prompt, then attend over those ids."""
+    sc = inputs.make_case(116, 64, 16, 2048, inputs.BF16, 131_072, 32, active_blocks=2048)
+    q, w, kb, nb = to_device(sc)
+    ws = qsa.alloc_workspace(64, 2048, 32, fused=True)
+    ids_c = torch.empty((64, 32), dtype=torch.int32, device="cuda")
+    ids_f = torch.empty_like(ids_c)
+    scores = torch.empty((64, 2048), dtype=torch.float32, device="cuda")
+    qsa.select(q, w, kb, nb, 32, ids_c, ws, scores=scores, active_blocks=2048)
+    qsa.select(q, w, kb, nb, 32, ids_f, ws, fused=True, active_blocks=2048)
+    assert torch.equal(ids_c, ids_f)
+    ids = ids_c.cpu().numpy()
+    c = inputs.make_attention_case(117, 64, 4, 131_072, sc.tokens, 32, ids=ids)
+    out, lse = _run(qsa, c, ids=ids_c)
+    rows = np.arange(0, 64, 4)
+    ref, ref_lse, wabs = attention_reference(c, rows)
+    check_rule_d(out[rows], lse[rows], ref, ref_lse, wabs)
+
+
+@pytest.fixture(scope="module")
+def deep_attention():
+    """The bench's configuration: 256 queries x 64 heads (4 GQA groups of 16),
+    capacity 524,288 tokens, contexts of 520,000 tokens, k = 32 random blocks."""
+    return inputs.deep_attention_case()
+
+
+def test_deep_prompt_sampled_queries(qsa, deep_attention):
+    c = deep_attention
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    rows = np.array([0, 1, 77, 128, 200, 255])
+    ref, ref_lse, wabs = attention_reference(c, rows)
+    check_rule_d(out[rows], lse[rows], ref, ref_lse, wabs)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    assert qsa.read_flags(ws) == 0
