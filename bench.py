@@ -13,7 +13,10 @@ better), the dominant kernel's roofline against MEASURED_PEAKS.json, the
 top-k and decode-window (3 queries, 258,000 tokens) figures, an end-to-end
 number through the C ABI with host buffers (H2D of the inputs and D2H of the
 ids inside the timed region), SM clocks sampled during the timed region, and
-the CPU oracle timed on a bounded sample of the same workload.
+the CPU oracle timed on a bounded sample of the same workload.  The selection
+attention over the timed call's ids (64 heads in 4 GQA groups of 16, K and V
+caches of 524,288 tokens) is timed beside it, with its own HBM roofline, and
+over the decode window's ids; it is not part of the step.
 
 ``--impl reference`` times the CPU oracle (the only reference this method has)
 on the host cores, each step a bounded sample of the same workload.
@@ -128,9 +131,10 @@ class ClockSampler:
 # The source files each timed kernel is compiled from; a committed DRAM-traffic
 # figure is reported only while all of them are unchanged.
 KERNEL_SOURCES = {
-    "fused": ("scorer_tc.cu", "warp_topk.cuh", "qsa_device.cuh"),
-    "scorer": ("scorer_tc.cu",),
+    "fused": ("scorer_tc.cu", "warp_topk.cuh", "qsa_device.cuh", "tc_ptx.cuh"),
+    "scorer": ("scorer_tc.cu", "tc_ptx.cuh"),
     "topk": ("topk.cu", "warp_topk.cuh", "qsa_device.cuh"),
+    "attention": ("sel_attn.cu", "tc_ptx.cuh", "qsa_device.cuh"),
 }
 
 
@@ -298,6 +302,31 @@ def cpu_baseline_all_cores(case, target_s=6.0):
                       f"scaled to the full call"}
 
 
+def attention_bytes(c) -> float:
+    """Algorithmic bytes of one selection-attention call: K and V of every selected
+    block of every (query, KV head) (2 x 64 x 128 bf16 = 32 KB), the queries, the
+    outputs, the lse, the ids and the context lengths, each read or written once."""
+    n_sel = int((c.ids >= 0).sum())
+    return (32768.0 * n_sel * c.n_kv_heads + c.nq * c.n_heads * (256.0 + 512.0 + 4.0)
+            + 4.0 * c.ids.size + 4.0 * c.nq)
+
+
+def attention_report(acase, adcase, us, us_dec, peaks, peak_src):
+    b = attention_bytes(acase)
+    gbs = b / (us * 1e-6) / 1e9
+    bd = attention_bytes(adcase)
+    gbs_d = bd / (us_dec * 1e-6) / 1e9
+    return {
+        "workload": acase.name, "ids": "the deep select call's ids (k = 32)",
+        "kernel": "sel_attn_kernel", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": gbs / peaks["hbm_gbs"], "traffic": profiled_traffic("attention"),
+        "per_launch": f"{b:.4g} B (32 KB of K and V per query, KV head and selected block; q, out, lse, ids)",
+        "us_per_launch": us, "l2": "flushed before every timed call", "peak_source": f"{peak_src} HBM copy",
+        "decode": {"workload": adcase.name, "us_per_call": us_dec, "bytes": bd, "gbs": gbs_d,
+                   "frac_of_hbm": gbs_d / peaks["hbm_gbs"]},
+    }
+
+
 def warm_us_per_call(torch, fn, calls, stream):
     """Back-to-back calls between one event pair (no flush): steady-state us per call."""
     fn()
@@ -400,6 +429,26 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in sections)
     d2h = hids.numel() * hids.element_size()
 
+    # selection attention over the select calls' own ids: 64 heads in 4 GQA groups of 16,
+    # K and V caches of the same capacity, contexts of the same length
+    select_chained()
+    decode_chained()
+    torch.cuda.synchronize()
+    acase = inputs.deep_attention_case(ids=ids.cpu().numpy())
+    a_dev = parity.attn_to_device(acase, dev)
+    a_out = torch.empty((acase.nq, acase.n_heads, 128), dtype=torch.float32, device=dev)
+    a_lse = torch.empty((acase.nq, acase.n_heads), dtype=torch.float32, device=dev)
+    adcase = inputs.decode_attention_case(ids=dids.cpu().numpy())
+    ad_dev = parity.attn_to_device(adcase, dev)
+    ad_out = torch.empty((adcase.nq, adcase.n_heads, 128), dtype=torch.float32, device=dev)
+    ad_lse = torch.empty((adcase.nq, adcase.n_heads), dtype=torch.float32, device=dev)
+
+    def attend():
+        qsa.select_attention(*a_dev, a_out, a_lse, scale=acase.scale)
+
+    def attend_decode():
+        qsa.select_attention(*ad_dev, ad_out, ad_lse, scale=adcase.scale)
+
     form = "fused"
     if args.profile_steps:
         # a fixed, short sequence of launches for ncu: both forms on both workloads
@@ -408,6 +457,8 @@ def run_ours(args):
             select_fused()
             decode_chained()
             decode_fused()
+            attend()
+            attend_decode()
         torch.cuda.synchronize()
         return 0
 
@@ -457,6 +508,8 @@ def run_ours(args):
     t_dec_f = timed_loop(torch, decode_fused, reps, flush, stream)
     t_dec_c = timed_loop(torch, decode_chained, reps, flush, stream)
     t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream, prime=False)
+    t_attn = timed_loop(torch, attend, 50, flush, stream)
+    t_attn_dec = timed_loop(torch, attend_decode, reps, flush, stream)
     # every top-k path forced on the same deep and decode scores (cold), and both select
     # forms back to back (warm)
     topk_paths = {}
@@ -519,6 +572,8 @@ def run_ours(args):
     us_dec_c = statistics.median(t_dec_c) * 1e3
     us_dec = min(us_dec_f, us_dec_c)
     us_e2e = statistics.mean(t_e2e) * 1e3
+    attn = attention_report(acase, adcase, statistics.median(t_attn) * 1e3, statistics.median(t_attn_dec) * 1e3,
+                            peaks, peak_src)
     line = {
         "metric": METRIC, "value": us_main, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_main, "higher_is_better": False, "scaling": "weak",
@@ -539,6 +594,7 @@ def run_ours(args):
                            "frac_of_hbm": dec_bytes / (us_dec * 1e-6) / 1e9 / peaks["hbm_gbs"]},
         "e2e": {"value": us_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "form": form},
+        "selection_attention": attn,
         "topk_paths_us_cold": topk_paths,
         "warm_back_to_back_us_per_call": warm,
         "gpu_launches": args.steps * (1 if form == "fused" else 1 + topk_launches),
