@@ -27,7 +27,14 @@
 // operands of both products are K-major under the 128-byte swizzle that TMA
 // writes.  Warp 0 issues TMA loads (K pairs, then V pairs, through one ring),
 // warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax and the
-// epilogue.  Every wait is bounded; on expiry the CTA raises
+// epilogue.
+//
+// When the (query, KV head) units are too few to fill the GPU (a decode
+// window), each unit's pairs are split over a thread-block cluster of 2, 4 or 8
+// CTAs.  Each CTA keeps its slice's unnormalised output, per-head maximum and
+// weight sum in shared memory; after a cluster barrier every CTA combines a
+// share of the group's heads from all partials, read through distributed shared
+// memory (weights 2^((m_r - M) scale log2 e), M the largest partial maximum).  Every wait is bounded; on expiry the CTA raises
 // QSA_FLAG_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -88,8 +95,10 @@ struct AttnParams {
     float *lse;
     uint32_t *flags;
     int n_heads, n_kv, k, capacity, nb_cap;
+    int split;                           // CTAs per (query, KV head): 1, or a cluster of 2, 4 or 8
     float scale, scale_log2;
 };
+constexpr int kMaxSplit = 8;
 
 __device__ __forceinline__ void soft_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -98,6 +107,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
     return __shfl_sync(kFull, ok, 0) != 0;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Barrier over every thread of the cluster; release/acquire orders shared-memory
+// writes before it with reads by other CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store to the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void *local, int rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ void st_cluster(float4 *local, int rank, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr(local, rank)), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster(float2 *local, int rank, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(cluster_addr(local, rank)), "f"(v.x), "f"(v.y)
+                 : "memory");
 }
 
 // Byte offset of (row, col) of a bf16 tile with 128-byte rows under the 128-byte swizzle.
@@ -132,7 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     AttnCtrl &ct = *reinterpret_cast<AttnCtrl *>(smem + kOffCtrl);
     volatile int *abort_flag = &ct.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qi = blockIdx.x / p.n_kv, g = blockIdx.x % p.n_kv;
+    const int split = p.split;                       // CTAs (one cluster) per (query, KV head)
+    const int rank = split > 1 ? (int)cluster_ctarank() : 0;
+    const int unit = blockIdx.x / split;
+    const int qi = unit / p.n_kv, g = unit % p.n_kv;
     const int head0 = g * kG;
 
     if (tid == 32) {
@@ -164,14 +202,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sQ + hh * kG * 128, &tm_q, &ct.qfull, hh * 64, qi * p.n_heads + head0);
     }
     if (warp == 2) {
-        // the query's distinct ids inside its context, in slot order
+        // the query's distinct ids inside its context, in slot order (both loads in
+        // flight before either is used)
+        const int32_t *row_ids = p.ids + (size_t)qi * p.k;
+        const int32_t r0 = lane < p.k ? row_ids[lane] : -1;
+        const int32_t r1 = lane + 32 < p.k ? row_ids[lane + 32] : -1;
         int ntok = p.n_tokens[qi];
         if (ntok < 0 || ntok > p.capacity) {
-            if (lane == 0 && g == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
+            if (lane == 0 && g == 0 && rank == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
             ntok = ntok < 0 ? 0 : p.capacity;
         }
         const int nb = (ntok + 63) >> 6;
-        for (int j = lane; j < p.k; j += 32) ct.raw[j] = p.ids[(size_t)qi * p.k + j];
+        ct.raw[lane] = r0;
+        ct.raw[lane + 32] = r1;
         __syncwarp();
         int cnt = 0;
         bool bad = false;
@@ -185,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (take) ct.sel[cnt + __popc(m & ((1u << lane) - 1u))] = b;
             cnt += __popc(m);
         }
-        if (__any_sync(kFull, bad) && lane == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_BAD_ID);
+        if (__any_sync(kFull, bad) && lane == 0 && rank == 0 && p.flags) atomicOr(p.flags, QSA_FLAG_BAD_ID);
         if (lane == 0) {
             ct.nsel = cnt;
             ct.ntok = ntok;
@@ -193,18 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const int nsel = ct.nsel, ntok = ct.ntok;
-    const int T = (nsel + 1) >> 1;   // pair tiles
+    // this CTA's pair tiles: all of them, or a slice of a cluster's split
+    const int T = (nsel + 1) >> 1;
+    const int p0 = rank * T / split, p1 = (rank + 1) * T / split;
+    const int tl = p1 - p0;
+    const int b0 = 2 * p0;                          // first block of the slice (index into sel)
+    const int nloc = min(nsel, 2 * p1) - b0;        // blocks of the slice
     float *out = p.out + ((size_t)qi * p.n_heads + head0) * 128;
-    if (nsel == 0) {   // no visible token: o = 0, lse = -inf
-        if (warp >= 2) {
-            for (int i = tid - 64; i < kG * 128; i += kSoft) out[i] = 0.0f;
-            if (p.lse && tid - 64 < kG) p.lse[(size_t)qi * p.n_heads + head0 + tid - 64] = -INFINITY;
-        }
-        if (tid == 0) mbar_drain(&ct.qfull, 0);
-        return;
-    }
+    float *lse = p.lse ? p.lse + (size_t)qi * p.n_heads + head0 : nullptr;
+    float *part = reinterpret_cast<float *>(sKV);   // split: this CTA's unnormalised output [16][128]
+
+    if (nloc > 0) {
     uint32_t ncols = 32;
-    while ((int)ncols < T * 16) ncols <<= 1;
+    while ((int)ncols < tl * 16) ncols <<= 1;
     if (warp == 1) {
         tmem_alloc(&ct.tmem_base, ncols);
         tmem_relinquish();
@@ -215,41 +259,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = ct.tmem_base;
 
     if (warp == 0) {
-        // ---------------- producer: K pairs 0..T-1, then V pairs 0..T-1.  Lane 0
+        // ---------------- producer: K pairs 0..tl-1, then V pairs 0..tl-1.  Lane 0
         // issues; the whole warp clears the V tokens past the context of the block
         // that holds its end, after that block lands and before the stage is
         // released to the MMA (its weights are 0, but 0 x NaN would not be).
         int issued = 0;
         bool tail_issued = false;
-        for (int i = 0; i < 2 * T; ++i) {
+        for (int i = 0; i < 2 * tl; ++i) {
             const int s = i % kStages;
             if (!warp_wait(&ct.empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort_flag)) break;
-            const int tile = i < T ? i : i - T;
-            const int nb_t = min(2, nsel - 2 * tile);
+            const int tile = i < tl ? i : i - tl;
+            const int nb_t = min(2, nloc - 2 * tile);
+            const int32_t *blk = ct.sel + b0 + 2 * tile;
             uint8_t *st = sKV + s * kStageBytes;
             int tail_j = -1;
-            if (i >= T)
+            if (i >= tl)
                 for (int j = 0; j < nb_t; ++j)
-                    if ((ct.sel[2 * tile + j] + 1) * 64 > ntok) tail_j = j;
+                    if ((blk[j] + 1) * 64 > ntok) tail_j = j;
             if (lane == 0) {
                 mbar_expect_tx(&ct.full[s], (uint32_t)((nb_t - (tail_j >= 0 ? 1 : 0)) * 16384));   // arrival 1
                 if (tail_j >= 0) mbar_expect_tx(&ct.tailbar, 16384u);
                 for (int j = 0; j < nb_t; ++j) {
-                    const int b = ct.sel[2 * tile + j];
-                    if (i < T) {   // 64 token rows, two 64-column halves of 16 KB regions
-                        const int y = g * p.capacity + b * 64;
+                    if (i < tl) {   // 64 token rows, two 64-column halves of 16 KB regions
+                        const int y = g * p.capacity + blk[j] * 64;
                         tma_load_2d(st + j * 8192, &tm_k, &ct.full[s], 0, y);
                         tma_load_2d(st + 16384 + j * 8192, &tm_k, &ct.full[s], 64, y);
-                    } else {       // 128 dimension rows of 64 tokens
+                    } else {        // 128 dimension rows of 64 tokens
                         tma_load_2d(st + j * 16384, &tm_v, j == tail_j ? &ct.tailbar : &ct.full[s], 0,
-                                    (g * p.nb_cap + b) * 128);
+                                    (g * p.nb_cap + blk[j]) * 128);
                     }
                 }
             }
             if (tail_j >= 0) {   // at most one block per query holds the end of its context
                 tail_issued = true;
-                if (warp_wait(&ct.tailbar, 0, abort_flag))
-                    clear_tail(st + tail_j * 16384, ntok - ct.sel[2 * tile + tail_j] * 64);
+                if (warp_wait(&ct.tailbar, 0, abort_flag)) clear_tail(st + tail_j * 16384, ntok - blk[tail_j] * 64);
                 fence_proxy_async();
                 __syncwarp();
             }
@@ -269,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(&ct.qfull, 0, abort_flag);
             tc_fence_after();
             const uint32_t q0 = smem_u32(sQ);
-            for (int i = 0; ok && i < T; ++i) {   // logits of pair i -> columns 16 i
+            for (int i = 0; ok && i < tl; ++i) {   // logits of pair i -> columns 16 i
                 const int s = i % kStages;
                 if (!(ok = mbar_wait(&ct.full[s], (uint32_t)(i / kStages) & 1u, abort_flag))) break;
                 tc_fence_after();
@@ -281,17 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&ct.empty[s]);
             }
             if (ok) mma_commit(&ct.sfull);
-            for (int i = 0; ok && i < T; ++i) {   // output: columns 0..15, after pair 0 is consumed
-                const int r = T + i, s = r % kStages, ps = i % kPStages;
+            for (int i = 0; ok && i < tl; ++i) {   // output: columns 0..15, after pair 0 is consumed
+                const int r = tl + i, s = r % kStages, ps = i % kPStages;
                 if (!(ok = mbar_wait(&ct.full[s], (uint32_t)(r / kStages) & 1u, abort_flag))) break;
                 if (!(ok = mbar_wait(&ct.pfull[ps], (uint32_t)(i / kPStages) & 1u, abort_flag))) break;
                 tc_fence_after();
-                const int nb_t = min(2, nsel - 2 * i);
-                const uint32_t a0 = smem_u32(sKV + s * kStageBytes), b0 = smem_u32(sP + ps * kPBytes);
+                const int nb_t = min(2, nloc - 2 * i);
+                const uint32_t a0 = smem_u32(sKV + s * kStageBytes), bp = smem_u32(sP + ps * kPBytes);
                 for (int j = 0; j < nb_t; ++j)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma<false>(tmem, sdesc(a0 + j * 16384 + kk * 32), sdesc(b0 + j * 2048 + kk * 32), id,
+                        mma<false>(tmem, sdesc(a0 + j * 16384 + kk * 32), sdesc(bp + j * 2048 + kk * 32), id,
                                    (i | j | kk) != 0 ? 1u : 0u);
                 mma_commit(&ct.empty[s]);
                 mma_commit(&ct.pempty[ps]);
@@ -311,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         auto visible = [&](int i) {
             const int j = 2 * i + half;
-            return j < nsel && ct.sel[j] * 64 + tok < ntok;
+            return j < nloc && ct.sel[b0 + j] * 64 + tok < ntok;
         };
         bool ok = warp_wait(&ct.sfull, 0, abort_flag);
         tc_fence_after();
@@ -319,16 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < kG; ++h) mx[h] = -INFINITY;
         if (ok) {
-            for (int i0 = 0; i0 < T; i0 += 4) {
+            for (int i0 = 0; i0 < tl; i0 += 4) {
                 uint32_t v[4][16];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    if (i0 + u < T) tmem_ld16_nowait(lane_addr + (uint32_t)((i0 + u) * 16), v[u]);
+                    if (i0 + u < tl) tmem_ld16_nowait(lane_addr + (uint32_t)((i0 + u) * 16), v[u]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     reg_fence(v[u]);
-                    if (i0 + u < T && visible(i0 + u))
+                    if (i0 + u < tl && visible(i0 + u))
 #pragma unroll
                         for (int h = 0; h < kG; ++h) mx[h] = fmaxf(mx[h], __uint_as_float(v[u][h]));
                 }
@@ -353,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l[kG];
 #pragma unroll
         for (int h = 0; h < kG; ++h) l[h] = 0.0f;
-        for (int i = 0; ok && i < T; ++i) {
+        for (int i = 0; ok && i < tl; ++i) {
             const int ps = i % kPStages;
             if (i >= kPStages && !(ok = warp_wait(&ct.pempty[ps], (uint32_t)((i / kPStages) - 1) & 1u, abort_flag)))
                 break;
@@ -362,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16_nowait(lane_addr + (uint32_t)(i * 16), v);
             tmem_wait_ld();
             reg_fence(v);
-            if (2 * i + half < nsel) {   // this row's block exists: write its weights (0 past the context)
+            if (2 * i + half < nloc) {   // this row's block exists: write its weights (0 past the context)
                 const bool vis = visible(i);
                 uint8_t *pb = sP + ps * kPBytes + half * 2048;
 #pragma unroll
@@ -397,10 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             reg_fence(o);
             // row = head dimension d; a warp's stores for one head are 32 consecutive floats
+            if (split == 1) {
 #pragma unroll
-            for (int h = 0; h < kG; ++h) out[h * 128 + row] = __uint_as_float(o[h]) / ct.l[h];
-            if (p.lse && row < kG)
-                p.lse[(size_t)qi * p.n_heads + head0 + row] = p.scale * ct.m[row] + logf(ct.l[row]);
+                for (int h = 0; h < kG; ++h) out[h * 128 + row] = __uint_as_float(o[h]) / ct.l[h];
+                if (lse && row < kG) lse[row] = p.scale * ct.m[row] + logf(ct.l[row]);
+            } else {   // the ring is idle once the output is complete
+#pragma unroll
+                for (int h = 0; h < kG; ++h) part[h * 128 + row] = __uint_as_float(o[h]);
+            }
         }
         tc_fence_before();
     }
@@ -410,7 +457,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
     }
+    } else {   // no visible token in this CTA's slice
+        if (split == 1 && warp >= 2) {   // o = 0, lse = -inf
+            for (int i = tid - 64; i < kG * 128; i += kSoft) out[i] = 0.0f;
+            if (lse && tid - 64 < kG) lse[tid - 64] = -INFINITY;
+        }
+        if (tid < kG) {
+            ct.m[tid] = -INFINITY;
+            ct.l[tid] = 0.0f;
+        }
+        if (tid == 0) mbar_drain(&ct.qfull, 0);
+    }
     if (tid == 0 && ct.abort && p.flags) atomicOr(p.flags, QSA_FLAG_WAIT_TIMEOUT);
+    if (split > 1) {
+        // Every CTA of the cluster is past its last MMA and copy, so every ring is
+        // idle.  Each CTA sends its partial (m, l and the unnormalised output of each
+        // head) to the CTA that combines that head, into the second ring stage of the
+        // receiver; after the second barrier every combine reads local memory only.
+        const int nh = kG / split;                                   // heads combined per CTA
+        float *recv = reinterpret_cast<float *>(sKV + kStageBytes);  // [split][nh][128]
+        float *recv_ml = recv + kG * 128;                            // [split][nh][2]
+        cluster_sync();
+        for (int e = tid; e < kG * 32; e += kThreads) {              // float4 e of part: head e / 32
+            const int h = e >> 5, d4 = e & 31;
+            const float4 v = reinterpret_cast<const float4 *>(part)[e];
+            st_cluster(reinterpret_cast<float4 *>(recv + ((rank * nh + h % nh) * 128)) + d4, h / nh, v);
+        }
+        if (tid < kG) {
+            const float2 ml = make_float2(ct.m[tid], ct.l[tid]);
+            st_cluster(reinterpret_cast<float2 *>(recv_ml) + rank * nh + tid % nh, tid / nh, ml);
+        }
+        cluster_sync();
+        for (int e = tid; e < nh * 128; e += kThreads) {
+            const int hh = e >> 7, d = e & 127;
+            const float2 *ml = reinterpret_cast<const float2 *>(recv_ml);
+            float M = -INFINITY;
+            for (int r = 0; r < split; ++r) M = fmaxf(M, ml[r * nh + hh].x);
+            float L = 0.0f, acc = 0.0f;
+            for (int r = 0; r < split; ++r) {
+                const float2 v = ml[r * nh + hh];
+                if (v.y > 0.0f) {   // a partial with no visible token has l = 0 and is skipped
+                    const float f = exp2f((v.x - M) * p.scale_log2);
+                    L = fmaf(f, v.y, L);
+                    acc = fmaf(f, recv[(r * nh + hh) * 128 + d], acc);
+                }
+            }
+            const int h = rank * nh + hh;
+            out[h * 128 + d] = L > 0.0f ? acc / L : 0.0f;
+            if (lse && d == 0) lse[h] = L > 0.0f ? p.scale * M + logf(L) : -INFINITY;
+        }
+    }
 }
 
 template <int Bytes>
@@ -432,8 +528,23 @@ qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
             opted_in[dev] = true;
         }
     }
-    sel_attn_kernel<<<grid, kThreads, Bytes, s>>>(mq, mk, mv, ap);
-    return check_cuda(cudaGetLastError(), "sel_attn_kernel launch");
+    if (ap.split == 1) {
+        sel_attn_kernel<<<grid, kThreads, Bytes, s>>>(mq, mk, mv, ap);
+        return check_cuda(cudaGetLastError(), "sel_attn_kernel launch");
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ap.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, sel_attn_kernel, mq, mk, mv, ap), "sel_attn_kernel cluster launch");
 }
 
 }  // namespace
@@ -459,10 +570,19 @@ qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s) {
     ap.nb_cap = a.capacity / 64;
     ap.scale = a.scale;
     ap.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
-    const int grid = a.nq * a.n_kv_heads;
-    // k > 32 blocks can take all 512 TMEM columns: one CTA per SM
-    return a.k > 32 ? launch_with<kSmemOneBytes>(mq, mk, mv, ap, grid, s)
-                    : launch_with<kSmemBytes>(mq, mk, mv, ap, grid, s);
+    // Few (query, KV head) units (a decode window): split each unit's pairs over a
+    // cluster of up to 8 CTAs, doubling while the grid stays within two CTAs per SM
+    // (clusters of 16, measured on the 3-query decode window, start further apart and
+    // finish later).
+    const int units = a.nq * a.n_kv_heads;
+    const int pairs = (a.k + 1) / 2;
+    ap.split = 1;
+    while (ap.split < kMaxSplit && ap.split * 2 <= pairs && (long)units * ap.split * 2 <= 2L * num_sms())
+        ap.split *= 2;
+    const int grid = units * ap.split;
+    // more than 32 blocks in one CTA can take all 512 TMEM columns: one CTA per SM
+    return a.k > 32 && ap.split == 1 ? launch_with<kSmemOneBytes>(mq, mk, mv, ap, grid, s)
+                                     : launch_with<kSmemBytes>(mq, mk, mv, ap, grid, s);
 }
 
 }  // namespace qsa

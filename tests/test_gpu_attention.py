@@ -76,6 +76,21 @@ def test_matches_oracle(qsa, params):
     assert qsa.read_flags(ws) == 0
 
 
+def test_split_and_unsplit_forms_both_match(qsa):
+    """80 queries x 2 KV heads fill the GPU (one CTA per unit); 4 of them alone are
+    split over clusters of CTAs that combine their partials: both match the oracle."""
+    c = _case(109, 80, 2, 4096, "ragged", 32, None)
+    full, full_lse = _run(qsa, c)
+    rows = np.arange(4)
+    sub = inputs.AttnCase(qa=c.qa[rows], kc=c.kc, vc=c.vc, ids=c.ids[rows], n_tokens=c.n_tokens[rows],
+                          scale=c.scale)
+    part, part_lse = _run(qsa, sub)
+    ref, ref_lse, wabs = attention_reference(c, rows)
+    check_rule_d(full[rows], full_lse[rows], ref, ref_lse, wabs)
+    check_rule_d(part, part_lse, ref, ref_lse, wabs)
+    assert not np.array_equal(part, full[rows])   # two different reductions
+
+
 def test_without_lse_or_workspace_the_output_is_the_same(qsa):
     c = _case(*CASES[1])
     a, _ = _run(qsa, c, _ws(qsa))
