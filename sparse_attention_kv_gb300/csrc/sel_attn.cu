@@ -32,10 +32,13 @@
 // When the (query, KV head) units are too few to fill the GPU (a decode
 // window), each unit's pairs are split over a thread-block cluster of 2, 4 or 8
 // CTAs.  Each CTA keeps its slice's unnormalised output, per-head maximum and
-// weight sum in shared memory; after a cluster barrier every CTA combines a
-// share of the group's heads from all partials, read through distributed shared
-// memory (weights 2^((m_r - M) scale log2 e), M the largest partial maximum).  Every wait is bounded; on expiry the CTA raises
-// QSA_FLAG_WAIT_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+// weight sum; after a cluster barrier it stores them through distributed shared
+// memory into the CTA that combines each head, and after a second barrier every
+// CTA combines its share of the group's heads from local memory (weights
+// 2^((m_r - M) scale log2 e), M the largest partial maximum).
+//
+// Every wait is bounded; on expiry the CTA raises QSA_FLAG_WAIT_TIMEOUT, drains
+// its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
