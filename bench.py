@@ -311,9 +311,18 @@ def attention_bytes(c) -> float:
             + 4.0 * c.ids.size + 4.0 * c.nq)
 
 
+def attention_unique_bytes(c) -> float:
+    """K and V bytes of the distinct blocks the whole call selects (every KV head reads
+    the same block ids): the traffic if each block were read from HBM once."""
+    ids = c.ids[c.ids >= 0]
+    return 32768.0 * len(np.unique(ids)) * c.n_kv_heads
+
+
 def attention_report(acase, adcase, us, us_dec, peaks, peak_src):
     b = attention_bytes(acase)
     gbs = b / (us * 1e-6) / 1e9
+    bu = attention_unique_bytes(acase)
+    traffic = profiled_traffic("attention")
     bd = attention_bytes(adcase)
     gbs_d = bd / (us_dec * 1e-6) / 1e9
     return {
@@ -322,6 +331,10 @@ def attention_report(acase, adcase, us, us_dec, peaks, peak_src):
         "frac": gbs / peaks["hbm_gbs"], "traffic": profiled_traffic("attention"),
         "per_launch": f"{b:.4g} B (32 KB of K and V per query, KV head and selected block; q, out, lse, ids)",
         "us_per_launch": us, "l2": "flushed before every timed call", "peak_source": f"{peak_src} HBM copy",
+        "note": "the algorithmic bytes count one 32 KB block read per (query, KV head, selected block); queries "
+                "that select the same block share it through L2, so DRAM moves less",
+        "bytes_unique_blocks": bu, "frac_unique_blocks": bu / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+        "dram_frac_from_traffic": None if traffic is None else traffic / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
         "decode": {"workload": adcase.name, "us_per_call": us_dec, "bytes": bd, "gbs": gbs_d,
                    "frac_of_hbm": gbs_d / peaks["hbm_gbs"]},
     }
