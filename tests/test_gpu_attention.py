@@ -1,7 +1,8 @@
 """Selection attention on the GPU against the FP64 oracle (parity rule (d)).
 
 Small cases span several pair tiles, odd block counts, pads, ragged contexts
-with partial tail blocks, k = 1 .. 64 (the one-CTA-per-SM form above 32),
+with partial tail blocks, k = 1 .. 64 (the one-CTA-per-SM form above 32), one
+unit per CTA and units split over clusters, grids of more CTAs than the GPU holds,
 several GQA groups, unsorted and repeated ids, ids past the context, NaN in the
 cache rows past the context, empty token sets, and the ids the select path
 itself produces.  The bench's configuration (256 queries x 64 heads in 4 GQA
@@ -68,6 +69,24 @@ def _case(seed, nq, n_kv, cap, tokens, k, n_valid):
 
 @pytest.mark.parametrize("params", CASES, ids=[f"nq{c[1]}-kv{c[2]}-C{c[3]}-{c[4]}-k{c[5]}" for c in CASES])
 def test_matches_oracle(qsa, params):
+    c = _case(*params)
+    ws = _ws(qsa)
+    out, lse = _run(qsa, c, ws)
+    ref, ref_lse, wabs = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, wabs)
+    assert qsa.read_flags(ws) == 0
+
+
+WAVE_CASES = [
+    # 320 units: more CTAs than the GPU holds at once (two per SM), with random pads
+    # and empty rows among them
+    (131, 80, 4, 4096, "ragged", 32, "random"),
+    (132, 40, 8, 2048, "ragged", 7, None),
+]
+
+
+@pytest.mark.parametrize("params", WAVE_CASES, ids=[f"nq{c[1]}-kv{c[2]}-k{c[5]}" for c in WAVE_CASES])
+def test_more_units_than_resident_ctas_match_oracle(qsa, params):
     c = _case(*params)
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
