@@ -10,8 +10,8 @@ Functions
 ---------
 block_scores(q, w, kblk, n_blocks, dtype)
     Double-precision block scores, ``[nq, max_blocks]`` (entries at
-    ``b >= n_blocks[q]`` are 0).  ``q``/``kblk`` are float32 arrays or, for
-    bf16, uint16 arrays holding the bf16 bit patterns.
+    ``b >= n_blocks[q]`` are 0).  ``q``/``kblk`` are float32 arrays, or the bit
+    patterns of bf16 (uint16) or fp8 e4m3 (uint8).
 select(scores, n_blocks, k)
     Per-query top-k over double scores: ids ascending, ties to the lower
     block id, -1 padded.
@@ -42,6 +42,8 @@ _lib = None
 
 F32 = 0
 BF16 = 1
+E4M3 = 2
+_STORAGE = {F32: np.float32, BF16: np.uint16, E4M3: np.uint8}
 
 
 def build(force: bool = False) -> str:
@@ -89,11 +91,11 @@ def _ptr(a: np.ndarray, ctype):
 
 def block_scores(q: np.ndarray, w: np.ndarray, kblk: np.ndarray, n_blocks: np.ndarray,
                  dtype: int | None = None) -> np.ndarray:
-    """Scores in double; q [nq,H,D], w [nq,H] fp32, kblk [C,D]; fp32 or bf16 bits (uint16)."""
+    """Scores in double; q [nq,H,D], w [nq,H] fp32, kblk [C,D]; fp32, or bf16 (uint16) / e4m3 (uint8) bits."""
     lib = _load()
     if dtype is None:
-        dtype = BF16 if q.dtype == np.uint16 else F32
-    want = np.uint16 if dtype == BF16 else np.float32
+        dtype = {np.dtype(np.uint16): BF16, np.dtype(np.uint8): E4M3}.get(np.asarray(q).dtype, F32)
+    want = _STORAGE[dtype]
     q = np.ascontiguousarray(q, dtype=want)
     kblk = np.ascontiguousarray(kblk, dtype=want)
     w = np.ascontiguousarray(w, dtype=np.float32)

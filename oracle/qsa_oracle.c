@@ -12,8 +12,8 @@
  * scorer of "#1091 qsa_select: FP32 tiled block scores below sm_80" (section
  * "What": rows are query x indexer head, the reduction runs over the head
  * dimension K = 128, and the ReLU of each head is weighted and summed per
- * block).  Inputs are read from the same fp32 or bf16 bits the GPU reads and
- * widened exactly (bf16 -> fp32 -> double are both exact), so every product is
+ * block).  Inputs are read from the same fp32, bf16 or fp8 e4m3 bits the GPU
+ * reads and widened exactly (each is a subset of double), so every product is
  * exact in double and the only rounding is in the 128-term and H-term sums.
  *
  * The selection keeps, per query, the k blocks that come first in the order
@@ -40,11 +40,26 @@
 #include <string.h>
 #include <math.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
 
-/* Widen element i of an fp32 or bf16 array to double, exactly. */
+/* Widen element i of an fp32, bf16 or fp8 e4m3 array to double, exactly.  e4m3
+ * (the OCP 8-bit floating-point format E4M3): sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent 0 holds the subnormals m x 2^-6 / 8; the pattern
+ * with every exponent and mantissa bit set is NaN; there is no infinity. */
 static double widen(const void *base, int dtype, size_t i)
 {
+    if (dtype == ORACLE_E4M3) {
+        uint8_t b = ((const uint8_t *)base)[i];
+        int e = (b >> 3) & 0xF, m = b & 7;
+        double v;
+        if (e == 0xF && m == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)m, -9);
+        else
+            v = ldexp(8.0 + m, e - 10);
+        return (b & 0x80) ? -v : v;
+    }
     if (dtype == ORACLE_BF16) {
         uint16_t h = ((const uint16_t *)base)[i];
         uint32_t u = ((uint32_t)h) << 16;
@@ -73,7 +88,7 @@ int qsa_oracle_block_scores(const void *q, const float *w, const void *kblk, int
 {
     if (!q || !w || !kblk || !n_blocks || !out) return -1;
     if (nq < 0 || n_heads <= 0 || head_dim <= 0 || max_blocks < 0) return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) return -1;
     for (int qi = 0; qi < nq; ++qi) {
         int n = clamp_n(n_blocks[qi], max_blocks);
         for (int b = 0; b < max_blocks; ++b) {

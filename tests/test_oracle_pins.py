@@ -111,6 +111,36 @@ def test_exactly_rounded_sum_crosscheck():
     assert worst <= 1e-13 * np.abs(s).max()
 
 
+def _e4m3_values(codes):
+    """Values of e4m3 codes read through the scorer: one head, w = 1, q = +-1 on d0,
+    the codes in kblk[:, 0]; relu(q.k) for q = +1 and q = -1 give the value's two sides."""
+    kb = np.zeros((len(codes), 128), dtype=np.uint8)
+    kb[:, 0] = codes
+    n = np.array([len(codes)], np.int32)
+    w = np.ones((1, 1), np.float32)
+    pos, neg = np.zeros((1, 1, 128), np.uint8), np.zeros((1, 1, 128), np.uint8)
+    pos[0, 0, 0], neg[0, 0, 0] = 0x38, 0xB8            # +1.0 and -1.0
+    return oracle.block_scores(pos, w, kb, n, oracle.E4M3)[0] - oracle.block_scores(neg, w, kb, n, oracle.E4M3)[0]
+
+
+def test_e4m3_widening_spec_values():
+    # OCP 8-bit floating point specification, E4M3: bias 7, max normal S.1111.110 = 448,
+    # min normal S.0001.000 = 2^-6, max subnormal S.0000.111 = 0.875 x 2^-6, min
+    # subnormal S.0000.001 = 2^-9, 1.0 = S.0111.000
+    codes = [0x00, 0x80, 0x01, 0x07, 0x08, 0x38, 0x3C, 0x40, 0x7E, 0xFE, 0xB8, 0x81]
+    want = [0.0, 0.0, 2.0 ** -9, 0.875 * 2.0 ** -6, 2.0 ** -6, 1.0, 1.5, 2.0, 448.0, -448.0, -1.0, -(2.0 ** -9)]
+    np.testing.assert_array_equal(_e4m3_values(codes), want)
+
+
+def test_e4m3_widening_matches_torch_for_every_finite_code():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)   # 0x7F, 0xFF are NaN
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(_e4m3_values(codes), ref)
+
+
 def test_bf16_matches_widened_fp32():
     """Scores of bf16 bits equal the scores of their exact fp32 widening."""
     c = inputs.make_case(21, 2, 4, 30, inputs.BF16, 30 * 64, 8)
@@ -254,6 +284,9 @@ MUTANTS = {
                      "s += (double)w[(size_t)qi * n_heads] * relu;"),
     "bf16_wrong_shift": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
     "no_pad": ("for (int i = m; i < k; ++i) out[i] = -1;", "for (int i = m; i < k; ++i) out[i] = 0;"),
+    "e4m3_bias": ("v = ldexp(8.0 + m, e - 10);", "v = ldexp(8.0 + m, e - 9);"),
+    "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "e4m3_sign": ("return (b & 0x80) ? -v : v;", "return v;"),
 }
 
 
@@ -264,7 +297,7 @@ def test_pins_catch_planted_oracle_mistakes(tmp_path, golden_dir, monkeypatch):
     pins = [test_scores_hand_fixture, test_bf16_widening_fixture, test_relu_per_head_identities,
             test_exactly_rounded_sum_crosscheck, test_select_hand_fixture,
             test_select_brute_force_tiny, test_select_closed_forms,
-            test_select_64_levels_lowest_ids_on_boundary_level]
+            test_select_64_levels_lowest_ids_on_boundary_level, test_e4m3_widening_spec_values]
     for name, (old, new) in MUTANTS.items():
         assert old in src, name
         msrc = tmp_path / f"{name}.c"
