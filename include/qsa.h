@@ -62,7 +62,9 @@ typedef enum {
 
 typedef enum {
     QSA_F32 = 0,  /* IEEE binary32 */
-    QSA_BF16 = 1  /* bfloat16 (upper half of a binary32) */
+    QSA_BF16 = 1, /* bfloat16 (upper half of a binary32) */
+    QSA_E4M3 = 2  /* 8-bit floating point E4M3 of the OCP FP8 specification (sign, 4 exponent bits
+                     with bias 7, 3 mantissa bits; no infinities, S.1111.111 = NaN) */
 } qsa_dtype;
 
 /* Top-k path.  AUTO picks from host-visible sizes only; the others force a path
@@ -108,7 +110,7 @@ qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
 /*
  * Block scores: scores[q * scores_stride + b] for 0 <= b < n_blocks[q].
  *
- *   q        [nq][n_heads][128]  dtype `dt` (fp32 or bf16), row-major, 16-byte aligned
+ *   q        [nq][n_heads][128]  dtype `dt` (fp32, bf16 or fp8 e4m3), row-major, 16-byte aligned
  *   w        [nq][n_heads]       fp32
  *   kblk     [max_blocks][128]   dtype `dt`, row-major, 16-byte aligned
  *   n_blocks [nq]                int32 on the DEVICE: blocks in each query's context,
@@ -123,9 +125,11 @@ qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
  *   ws, ws_bytes                 workspace (may be NULL/0: then device flags are not
  *                                recorded)
  *
- * Arithmetic: products on the tensor cores (bf16 x bf16 -> fp32, or fp32 split in
- * three tf32 products), accumulated in fp32; ReLU and the head-weighted sum in
- * fp32.  n_heads must be 1, 2, 4, 8 or 16.
+ * Arithmetic: products on the tensor cores (bf16 x bf16 -> fp32, e4m3 x e4m3 ->
+ * fp32, or fp32 split in three tf32 products), accumulated in fp32; ReLU and the
+ * head-weighted sum in fp32.  n_heads must be 1, 2, 4, 8 or 16.  e4m3 stores the
+ * indexer keys (and queries) in 8 bits, as the pages' engine stores its KV cache
+ * in 8 bits ("--kv int8"); the tensor-core 8-bit format of this GPU is e4m3.
  * Errors: QSA_ERR_INVALID_ARG for NULL q/w/kblk/n_blocks/scores, nq < 1,
  * head_dim != 128, unsupported n_heads, max_blocks outside [1, QSA_MAX_BLOCKS],
  * scores_stride < max_blocks, misaligned q/kblk, bad dtype.

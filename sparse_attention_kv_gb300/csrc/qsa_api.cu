@@ -116,7 +116,7 @@ static qsa_status check_scorer_args(const void *q, const float *w, const void *k
     if (st != QSA_OK) return st;
     if (!q || !w || !kblk || !n_blocks) return fail(QSA_ERR_INVALID_ARG, "NULL q, w, kblk or n_blocks");
     if (scores_required && !scores) return fail(QSA_ERR_INVALID_ARG, "scores is NULL");
-    if (dt != QSA_F32 && dt != QSA_BF16) return fail(QSA_ERR_INVALID_ARG, "bad dtype %d", dt);
+    if (dt != QSA_F32 && dt != QSA_BF16 && dt != QSA_E4M3) return fail(QSA_ERR_INVALID_ARG, "bad dtype %d", dt);
     if (head_dim != QSA_HEAD_DIM)
         return fail(QSA_ERR_INVALID_ARG, "head_dim must be %d (got %d)", QSA_HEAD_DIM, head_dim);
     if (n_heads != 1 && n_heads != 2 && n_heads != 4 && n_heads != 8 && n_heads != 16)

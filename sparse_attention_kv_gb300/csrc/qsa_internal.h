@@ -18,9 +18,10 @@ qsa_status check_cuda(cudaError_t err, const char *what);
 
 int num_sms();  // SM count of the current device (cached per device)
 
-// A 2-D TMA tensor map over a row-major [rows][inner] array (fp32 or bf16), box of
-// 128 bytes x box_rows, 128-byte swizzle; encoded once per (pointer, shape, device).
-qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint32_t inner, uint64_t rows, uint32_t box_rows);
+// A 2-D TMA tensor map over a row-major [rows][inner] array of esize-byte elements
+// (4: fp32, 2: bf16, 1: 8-bit), box of 128 bytes x box_rows, 128-byte swizzle;
+// encoded once per (pointer, shape, device).
+qsa_status get_map(CUtensorMap *out, const void *ptr, int esize, uint32_t inner, uint64_t rows, uint32_t box_rows);
 
 // Candidate slots per (query, chunk) are sized for chunks of at least this many blocks.
 constexpr int kMinChunk = 128;

@@ -14,7 +14,8 @@
 // shared-memory stages, the query-group tile once), warp 1 owns TMEM and issues
 // tcgen05.mma from one thread, warps 2-5 drain the double-buffered accumulator
 // (tcgen05.ld) and write the scores.  bf16 inputs use kind::f16 (bf16 x bf16 ->
-// fp32).  fp32 inputs use kind::tf32 on a three-term split a = a_hi + a_lo
+// fp32); fp8 e4m3 inputs use kind::f8f6f4 (e4m3 x e4m3 -> fp32, the 128 elements
+// of K in one 128-byte swizzle atom).  fp32 inputs use kind::tf32 on a three-term split a = a_hi + a_lo
 // (a_hi = a with the low 13 mantissa bits cleared): a_hi*b_hi + a_hi*b_lo +
 // a_lo*b_hi, which keeps the product error near 2^-20 relative.
 //
@@ -44,17 +45,25 @@ constexpr int kEpi = 128 * kEpiParts;         // epilogue threads
 constexpr int kThreads = 64 + kEpi;           // + one TMA warp and one MMA warp
 constexpr int kMaxChunks = (16 + kEpiParts - 1) / kEpiParts;  // 16-column chunks per thread
 
-template <bool F32>
+template <int DT>
 struct Cfg;
 template <>
-struct Cfg<false> {  // bf16 -> kind::f16
+struct Cfg<QSA_BF16> {  // bf16 -> kind::f16
     static constexpr int kEsize = 2, kEPA = 64, kAtoms = 2, kStages = 4, kMaxBN = 256;
     static constexpr uint32_t kFmt = 1;
+    static constexpr MmaKind kKind = MmaKind::f16;
 };
 template <>
-struct Cfg<true> {  // fp32 -> kind::tf32, three-term split
+struct Cfg<QSA_F32> {  // fp32 -> kind::tf32, three-term split
     static constexpr int kEsize = 4, kEPA = 32, kAtoms = 4, kStages = 1, kMaxBN = 64;
     static constexpr uint32_t kFmt = 2;
+    static constexpr MmaKind kKind = MmaKind::tf32;
+};
+template <>
+struct Cfg<QSA_E4M3> {  // fp8 e4m3 -> kind::f8f6f4, K = 128 in one 128-byte atom
+    static constexpr int kEsize = 1, kEPA = 128, kAtoms = 1, kStages = 4, kMaxBN = 256;
+    static constexpr uint32_t kFmt = 0;
+    static constexpr MmaKind kKind = MmaKind::f8f6f4;
 };
 
 // One 128-byte swizzle atom of a tile holds rows x 128 bytes (kEPA elements of K).
@@ -62,17 +71,18 @@ constexpr int kAtomA = kBM * 128;  // 16 KB
 
 // The fused kernel keeps each CTA's scores on chip (kSbuf bytes) and gives each
 // epilogue warp a 256-bin histogram; it pays for them with fewer kblk stages.
-template <bool F32, bool FUSED>
+template <int DT, bool FUSED>
 struct Layout {
-    using C = Cfg<F32>;
-    static constexpr int kStages = (FUSED && !F32) ? 2 : C::kStages;
+    using C = Cfg<DT>;
+    static constexpr bool kF32 = DT == QSA_F32;
+    static constexpr int kStages = (FUSED && !kF32) ? 2 : C::kStages;
     static constexpr int kB = C::kAtoms * C::kMaxBN * 128;
     static constexpr int kAStage = C::kAtoms * kAtomA;
     static constexpr int offB = 0;
     static constexpr int offBlo = offB + kB;
-    static constexpr int offA = offBlo + (F32 ? kB : 0);
+    static constexpr int offA = offBlo + (kF32 ? kB : 0);
     static constexpr int offAlo = offA + kStages * kAStage;
-    static constexpr int offCtrl = offAlo + (F32 ? kStages * kAStage : 0);
+    static constexpr int offCtrl = offAlo + (kF32 ? kStages * kAStage : 0);
 };
 constexpr int kHistBytes = (kEpi / 32) * 256 * 4;   // one 256-bin histogram per epilogue warp
 
@@ -88,13 +98,13 @@ struct Ctrl {
     int nb[256];
 };
 
-template <bool F32, bool FUSED>
+template <int DT, bool FUSED>
 constexpr int sbuf_bytes() {
-    return FUSED ? (227 * 1024 - 1024 - Layout<F32, FUSED>::offCtrl - (int)sizeof(Ctrl) - kHistBytes) / 1024 * 1024 : 0;
+    return FUSED ? (227 * 1024 - 1024 - Layout<DT, FUSED>::offCtrl - (int)sizeof(Ctrl) - kHistBytes) / 1024 * 1024 : 0;
 }
-template <bool F32, bool FUSED>
+template <int DT, bool FUSED>
 constexpr int smem_bytes() {
-    return Layout<F32, FUSED>::offCtrl + (int)sizeof(Ctrl) + (FUSED ? kHistBytes + sbuf_bytes<F32, FUSED>() : 0) + 1024;
+    return Layout<DT, FUSED>::offCtrl + (int)sizeof(Ctrl) + (FUSED ? kHistBytes + sbuf_bytes<DT, FUSED>() : 0) + 1024;
 }
 
 struct KParams {
@@ -314,12 +324,13 @@ __device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbu
 
 // ---------------------------------------------------------------- kernel
 
-template <bool F32, int H, bool FUSED>
+template <int DT, int H, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     scorer_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                      const KParams p) {
-    using C = Cfg<F32>;
-    using L = Layout<F32, FUSED>;
+    using C = Cfg<DT>;
+    using L = Layout<DT, FUSED>;
+    constexpr bool F32 = DT == QSA_F32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sB = smem + L::offB;
@@ -459,10 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t aoff = (uint32_t)(a * kAtomA + kk * 32);
                         const uint32_t boff = (uint32_t)(a * bn * 128 + kk * 32);
                         const uint32_t acc = (a | kk) != 0 ? 1u : 0u;
-                        mma<F32>(d, sdesc(a0 + aoff), sdesc(b0 + boff), id, acc);
+                        mma<C::kKind>(d, sdesc(a0 + aoff), sdesc(b0 + boff), id, acc);
                         if constexpr (F32) {
-                            mma<F32>(d, sdesc(a0 + aoff), sdesc(bl0 + boff), id, 1u);
-                            mma<F32>(d, sdesc(al0 + aoff), sdesc(b0 + boff), id, 1u);
+                            mma<C::kKind>(d, sdesc(a0 + aoff), sdesc(bl0 + boff), id, 1u);
+                            mma<C::kKind>(d, sdesc(al0 + aoff), sdesc(b0 + boff), id, 1u);
                         }
                     }
                 }
@@ -554,10 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <bool F32, int H, bool FUSED>
+template <int DT, int H, bool FUSED>
 qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
                         cudaStream_t s) {
-    constexpr int bytes = smem_bytes<F32, FUSED>();
+    constexpr int bytes = smem_bytes<DT, FUSED>();
     static_assert(bytes <= 227 * 1024, "scorer shared memory");
     // the shared-memory opt-in is a per-device property of the function: set it once on
     // every device this instantiation launches on
@@ -570,26 +581,26 @@ qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KPar
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!opted_in[dev]) {
-            st = check_cuda(cudaFuncSetAttribute(scorer_tc_kernel<F32, H, FUSED>,
+            st = check_cuda(cudaFuncSetAttribute(scorer_tc_kernel<DT, H, FUSED>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
                             "cudaFuncSetAttribute(scorer)");
             if (st != QSA_OK) return st;
             opted_in[dev] = true;
         }
     }
-    scorer_tc_kernel<F32, H, FUSED><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
+    scorer_tc_kernel<DT, H, FUSED><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
     return check_cuda(cudaGetLastError(), FUSED ? "fused scorer+select launch" : "scorer_tc_kernel launch");
 }
 
-template <bool F32, bool FUSED>
+template <int DT, bool FUSED>
 qsa_status launch_heads(int H, const CUtensorMap &mk, const CUtensorMap &mq, const KParams &kp, dim3 grid,
                         cudaStream_t s) {
     switch (H) {
-    case 1: return launch_typed<F32, 1, FUSED>(mk, mq, kp, grid, s);
-    case 2: return launch_typed<F32, 2, FUSED>(mk, mq, kp, grid, s);
-    case 4: return launch_typed<F32, 4, FUSED>(mk, mq, kp, grid, s);
-    case 8: return launch_typed<F32, 8, FUSED>(mk, mq, kp, grid, s);
-    case 16: return launch_typed<F32, 16, FUSED>(mk, mq, kp, grid, s);
+    case 1: return launch_typed<DT, 1, FUSED>(mk, mq, kp, grid, s);
+    case 2: return launch_typed<DT, 2, FUSED>(mk, mq, kp, grid, s);
+    case 4: return launch_typed<DT, 4, FUSED>(mk, mq, kp, grid, s);
+    case 8: return launch_typed<DT, 8, FUSED>(mk, mq, kp, grid, s);
+    case 16: return launch_typed<DT, 16, FUSED>(mk, mq, kp, grid, s);
     default: return fail(QSA_ERR_INVALID_ARG, "n_heads %d", H);
     }
 }
@@ -597,9 +608,9 @@ qsa_status launch_heads(int H, const CUtensorMap &mk, const CUtensorMap &mq, con
 }  // namespace
 
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
-    const bool f32 = a.dt == QSA_F32;
+    const int dt = a.dt;
     const int H = a.n_heads;
-    const int max_bn = f32 ? Cfg<true>::kMaxBN : Cfg<false>::kMaxBN;
+    const int max_bn = dt == QSA_F32 ? Cfg<QSA_F32>::kMaxBN : dt == QSA_E4M3 ? Cfg<QSA_E4M3>::kMaxBN : Cfg<QSA_BF16>::kMaxBN;
     const int tiles = (a.bound + kBM - 1) / kBM;
     if (tiles == 0 && !a.fused) return QSA_OK;   // no block can be valid
     const int sms = num_sms();
@@ -614,7 +625,9 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
         cpg = std::max(1, std::min(t1, sms / groups));
         tpc = (t1 + cpg - 1) / cpg;
         if (!a.fused) break;
-        const int sbuf = f32 ? sbuf_bytes<true, true>() : sbuf_bytes<false, true>();
+        const int sbuf = dt == QSA_F32    ? sbuf_bytes<QSA_F32, true>()
+                         : dt == QSA_E4M3 ? sbuf_bytes<QSA_E4M3, true>()
+                                          : sbuf_bytes<QSA_BF16, true>();
         const int tpc_max = sbuf / (qg * kBM * 4);
         bool fits = tpc_max >= 1;
         if (fits) {
@@ -635,9 +648,10 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     while (tmem_cols < 2 * bn) tmem_cols *= 2;
 
     CUtensorMap mk, mq;
-    qsa_status st = get_map(&mk, a.kblk, f32, QSA_HEAD_DIM, (uint64_t)a.max_blocks, kBM);
+    const int esize = dt == QSA_F32 ? 4 : dt == QSA_E4M3 ? 1 : 2;
+    qsa_status st = get_map(&mk, a.kblk, esize, QSA_HEAD_DIM, (uint64_t)a.max_blocks, kBM);
     if (st != QSA_OK) return st;
-    st = get_map(&mq, a.q, f32, QSA_HEAD_DIM, (uint64_t)a.nq * H, (uint32_t)bn);
+    st = get_map(&mq, a.q, esize, QSA_HEAD_DIM, (uint64_t)a.nq * H, (uint32_t)bn);
     if (st != QSA_OK) return st;
 
     KParams kp{};
@@ -660,9 +674,17 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     kp.maxch = a.maxch;
     kp.sb_stride = tpc * kBM;
     const dim3 grid(cpg, groups);
-    if (a.fused)
-        return f32 ? launch_heads<true, true>(H, mk, mq, kp, grid, s) : launch_heads<false, true>(H, mk, mq, kp, grid, s);
-    return f32 ? launch_heads<true, false>(H, mk, mq, kp, grid, s) : launch_heads<false, false>(H, mk, mq, kp, grid, s);
+    switch (dt) {
+    case QSA_F32:
+        return a.fused ? launch_heads<QSA_F32, true>(H, mk, mq, kp, grid, s)
+                       : launch_heads<QSA_F32, false>(H, mk, mq, kp, grid, s);
+    case QSA_E4M3:
+        return a.fused ? launch_heads<QSA_E4M3, true>(H, mk, mq, kp, grid, s)
+                       : launch_heads<QSA_E4M3, false>(H, mk, mq, kp, grid, s);
+    default:
+        return a.fused ? launch_heads<QSA_BF16, true>(H, mk, mq, kp, grid, s)
+                       : launch_heads<QSA_BF16, false>(H, mk, mq, kp, grid, s);
+    }
 }
 
 }  // namespace qsa

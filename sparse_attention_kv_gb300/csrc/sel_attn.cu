@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a0 = smem_u32(sKV + s * kStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma<false>(tmem + (uint32_t)(i * 16), sdesc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                    mma<MmaKind::f16>(tmem + (uint32_t)(i * 16), sdesc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32),
                                sdesc(q0 + (kk >> 2) * (kG * 128) + (kk & 3) * 32), id, kk > 0 ? 1u : 0u);
                 mma_commit(&ct.empty[s]);
             }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nb_t; ++j)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma<false>(tmem, sdesc(a0 + j * 16384 + kk * 32), sdesc(bp + j * 2048 + kk * 32), id,
+                        mma<MmaKind::f16>(tmem, sdesc(a0 + j * 16384 + kk * 32), sdesc(bp + j * 2048 + kk * 32), id,
                                    (i | j | kk) != 0 ? 1u : 0u);
                 mma_commit(&ct.empty[s]);
                 mma_commit(&ct.pempty[ps]);
@@ -554,11 +554,11 @@ qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
 
 qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s) {
     CUtensorMap mq, mk, mv;
-    qsa_status st = get_map(&mq, a.qa, false, QSA_HEAD_DIM, (uint64_t)a.nq * a.n_heads, kG);
+    qsa_status st = get_map(&mq, a.qa, 2, QSA_HEAD_DIM, (uint64_t)a.nq * a.n_heads, kG);
     if (st != QSA_OK) return st;
-    st = get_map(&mk, a.kcache, false, QSA_HEAD_DIM, (uint64_t)a.n_kv_heads * a.capacity, 64);
+    st = get_map(&mk, a.kcache, 2, QSA_HEAD_DIM, (uint64_t)a.n_kv_heads * a.capacity, 64);
     if (st != QSA_OK) return st;
-    st = get_map(&mv, a.vcache_t, false, 64, (uint64_t)a.n_kv_heads * a.capacity * 2, 128);
+    st = get_map(&mv, a.vcache_t, 2, 64, (uint64_t)a.n_kv_heads * a.capacity * 2, 128);
     if (st != QSA_OK) return st;
     AttnParams ap{};
     ap.ids = a.ids;

@@ -93,12 +93,22 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-template <bool F32>
+// tcgen05.mma kinds used here: bf16 x bf16, tf32 x tf32 and fp8 x fp8 (e4m3), all
+// accumulating in fp32.
+enum class MmaKind { f16, tf32, f8f6f4 };
+
+template <MmaKind KIND>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (F32) {
+    if constexpr (KIND == MmaKind::tf32) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+            : "memory");
+    } else if constexpr (KIND == MmaKind::f8f6f4) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
             : "memory");
     } else {
@@ -144,7 +154,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
-// Instruction descriptor: fp32 accumulator, A/B format `fmt`, both K-major, M x N.
+// Instruction descriptor: fp32 accumulator, A/B format `fmt` (kind::f16: 1 = bf16;
+// kind::tf32: 2; kind::f8f6f4: 0 = e4m3), both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, int M, int N) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

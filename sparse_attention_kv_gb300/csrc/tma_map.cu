@@ -1,6 +1,7 @@
-// tma_map.cu -- host side of the TMA tensor loads: 2-D tensor maps with a
-// 128-byte swizzle (the shared-memory layout the tcgen05 descriptors expect),
-// encoded through the driver entry point and cached per (pointer, shape, device).
+// tma_map.cu -- host side of the TMA tensor loads: 2-D tensor maps of fp32, bf16
+// or 8-bit elements with a 128-byte swizzle (the shared-memory layout the tcgen05
+// descriptors expect), encoded through the driver entry point and cached per
+// (pointer, shape, element size, device).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -30,10 +31,10 @@ struct MapKey {
     uint32_t inner;
     uint64_t rows;
     uint32_t box_rows;
-    int f32;
+    int esize;
     int dev;
     bool operator==(const MapKey &o) const {
-        return ptr == o.ptr && inner == o.inner && rows == o.rows && box_rows == o.box_rows && f32 == o.f32 &&
+        return ptr == o.ptr && inner == o.inner && rows == o.rows && box_rows == o.box_rows && esize == o.esize &&
                dev == o.dev;
     }
 };
@@ -41,14 +42,14 @@ struct MapKey {
 }  // namespace
 
 // Small cache of encoded tensor maps (a map is 128 bytes of host data).
-qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint32_t inner, uint64_t rows, uint32_t box_rows) {
+qsa_status get_map(CUtensorMap *out, const void *ptr, int esize, uint32_t inner, uint64_t rows, uint32_t box_rows) {
     static std::mutex mu;
     static MapKey keys[32];
     static CUtensorMap maps[32];
     static int used = 0, next = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    const MapKey key{ptr, inner, rows, box_rows, f32 ? 1 : 0, dev};
+    const MapKey key{ptr, inner, rows, box_rows, esize, dev};
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < used; ++i)
@@ -60,11 +61,15 @@ qsa_status get_map(CUtensorMap *out, const void *ptr, bool f32, uint32_t inner, 
     auto fn = encode_fn();
     if (!fn) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)inner * (f32 ? 4 : 2)};
-    const cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), box_rows};
+    if (esize != 1 && esize != 2 && esize != 4) return fail(QSA_ERR_INVALID_ARG, "element size %d", esize);
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), box_rows};
+    const CUtensorMapDataType dtype = esize == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const cuuint32_t estr[2] = {1, 1};
     CUtensorMap m;
-    const CUresult r = fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const CUresult r = fn(&m, dtype, 2,
                           const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -31,6 +31,7 @@ BLOCK_TOKENS = 64
 HEAD_DIM = 128
 F32 = 0
 BF16 = 1
+E4M3 = 2
 
 
 def blocks_for_tokens(tokens):
@@ -51,6 +52,31 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out.reshape(np.shape(x))
 
 
+def _e4m3_codes_values():
+    """Values of the non-negative finite e4m3 codes 0x00 .. 0x7E (ascending): OCP 8-bit
+    floating point E4M3, bias 7, exponent 0 holding the subnormals."""
+    codes = np.arange(0x7F, dtype=np.int64)
+    e, m = (codes >> 3) & 0xF, codes & 7
+    return np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e - 10.0))
+
+
+_E4M3_VALUES = _e4m3_codes_values()
+_E4M3_MIDS = (_E4M3_VALUES[:-1] + _E4M3_VALUES[1:]) / 2
+
+
+def to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e4m3 bit patterns (uint8): nearest value, ties to the even code,
+    magnitudes past 448 saturated to 448 (inputs are finite)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64).reshape(-1)
+    idx = np.searchsorted(_E4M3_MIDS, a, side="left")       # ties land on the lower code
+    tie = (idx < len(_E4M3_MIDS)) & (a == _E4M3_MIDS[np.minimum(idx, len(_E4M3_MIDS) - 1)])
+    idx = np.where(tie & (idx % 2 == 1), idx + 1, idx)
+    idx = np.minimum(idx, 0x7E)
+    sign = np.signbit(x).reshape(-1).astype(np.uint8) << 7
+    return (idx.astype(np.uint8) | sign).reshape(x.shape)
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> fp32 values (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
@@ -60,8 +86,8 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 class Case:
     """One synthetic selection problem.
 
-    ``q`` [nq,H,D] and ``kblk`` [C,D] hold fp32 values (dtype F32) or bf16 bit
-    patterns as uint16 (dtype BF16); ``w`` [nq,H] is fp32; ``n_blocks`` [nq]
+    ``q`` [nq,H,D] and ``kblk`` [C,D] hold fp32 values (dtype F32), bf16 bit
+    patterns as uint16 (dtype BF16) or fp8 e4m3 bit patterns as uint8 (dtype E4M3); ``w`` [nq,H] is fp32; ``n_blocks`` [nq]
     int32.  ``tokens`` is the per-query context length the blocks cover.
     """
     q: np.ndarray
@@ -109,6 +135,9 @@ def make_case(seed: int, nq: int, n_heads: int, capacity_blocks: int, dtype: int
     if dtype == BF16:
         q = to_bf16_bits(q)
         kblk = to_bf16_bits(kblk)
+    elif dtype == E4M3:
+        q = to_e4m3_bits(q)
+        kblk = to_e4m3_bits(kblk)
     return Case(q=q, w=w, kblk=kblk, n_blocks=n_blocks, tokens=toks, dtype=dtype, k=k,
                 active_blocks=active_blocks, name=name)
 
@@ -159,6 +188,18 @@ def deep_case(i: int) -> Case:
     nb = int(blocks_for_tokens(t))
     return make_case(4000 + i, 256, 16, 8192, BF16, t, 32, active_blocks=nb,
                      name=f"deep 256q x 16h bf16, {t:,} tokens, capacity 524,288")
+
+
+def deep_e4m3_case() -> Case:
+    """The deep prompt at 520,000 tokens with q and kblk stored as fp8 e4m3 (the same
+    N(0,1) draws as the bf16 case, rounded to e4m3)."""
+    return make_case(4002, 256, 16, 8192, E4M3, 520_000, 32, active_blocks=8125,
+                     name="deep 256q x 16h e4m3, 520,000 tokens, capacity 524,288")
+
+
+def decode_e4m3_case() -> Case:
+    return make_case(2005, 3, 16, 4096, E4M3, 258_000, 32,
+                     name="decode 3q x 16h e4m3, 258,000 tokens, capacity 262,144")
 
 
 def stress_case(kind: str) -> Case:

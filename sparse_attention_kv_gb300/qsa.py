@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libqsa.so")
 # qsa_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 # qsa_dtype
-F32, BF16 = 0, 1
+F32, BF16, E4M3 = 0, 1, 2
 # qsa_path
 PATH_AUTO, PATH_SPLIT, PATH_SAMPLE, PATH_REGISTER, PATH_RADIX, PATH_WARP = range(6)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SPLIT: "split", PATH_SAMPLE: "sample",
@@ -110,7 +110,9 @@ def _dtype_code(t: torch.Tensor, name: str) -> int:
         return BF16
     if t.dtype == torch.float32:
         return F32
-    raise ValueError(f"{name} must be bfloat16 or float32 (got {t.dtype})")
+    if t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return E4M3
+    raise ValueError(f"{name} must be bfloat16, float32 or float8_e4m3fn (got {t.dtype})")
 
 
 def _contig(t: torch.Tensor, name: str) -> None:
@@ -141,7 +143,8 @@ def auto_path(nq: int, max_blocks: int, active_blocks: int, k: int) -> int:
 def block_scores(q: torch.Tensor, w: torch.Tensor, kblk: torch.Tensor, n_blocks: torch.Tensor,
                  scores: torch.Tensor, active_blocks: int = -1, ws: torch.Tensor | None = None,
                  stream=None) -> torch.Tensor:
-    """scores[q, b] for b < n_blocks[q]; q [nq,H,128], w [nq,H] fp32, kblk [C,128]."""
+    """scores[q, b] for b < n_blocks[q]; q [nq,H,128], w [nq,H] fp32, kblk [C,128]
+    (q and kblk both float32, bfloat16 or float8_e4m3fn)."""
     lib = load()
     for t, nm in ((q, "q"), (w, "w"), (kblk, "kblk"), (n_blocks, "n_blocks")):
         _contig(t, nm)

@@ -24,7 +24,7 @@ from __future__ import annotations
 
 import numpy as np
 
-TOL = {0: 1e-4, 1: 1e-2}   # by dtype code: fp32, bf16
+TOL = {0: 1e-4, 1: 1e-2, 2: 1e-2}   # by dtype code: fp32, bf16, fp8 e4m3 (the low-precision rule)
 
 
 def to_device(case, device="cuda"):
@@ -32,6 +32,9 @@ def to_device(case, device="cuda"):
     if case.dtype == 1:
         q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16)
         kb = torch.from_numpy(case.kblk.view(np.int16)).view(torch.bfloat16)
+    elif case.dtype == 2:
+        q = torch.from_numpy(case.q).view(torch.float8_e4m3fn)
+        kb = torch.from_numpy(case.kblk).view(torch.float8_e4m3fn)
     else:
         q = torch.from_numpy(case.q)
         kb = torch.from_numpy(case.kblk)

@@ -79,7 +79,7 @@ def test_fused_stress(kind):
 
 
 @pytest.mark.parametrize("H", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16, inputs.E4M3])
 def test_fused_heads_dtypes_and_short_rows(H, dtype):
     """Every head count and input type; ragged rows including n = 0, 1, k-1, k, k+1."""
     nq, C, k = 37, 700, 24

@@ -96,10 +96,39 @@ def test_every_path_end_to_end_on_decode_and_prompt(path):
                 raise
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_e4m3_decode_window_chained_and_fused(fused):
+    case = inputs.decode_e4m3_case()
+    ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
+    ids, sc, flags = run_select(case, fused=fused)
+    assert flags & qsa.ERROR_FLAGS == 0
+    parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
+    parity.check_rule_a(ids, oracle.select_f32(sc, case.n_blocks, case.k))
+    parity.check_rule_c(ids, ref, oracle.select(ref, case.n_blocks, case.k), case.n_blocks, case.k, case.dtype)
+
+
+def test_e4m3_deep_prompt_sampled():
+    """fp8 q and kblk at 520,000 tokens: scores and ids of 32 sampled queries against
+    the oracle, both select forms, and the fused ids equal to the chained ones."""
+    case = inputs.deep_e4m3_case()
+    ids, sc, flags = run_select(case)
+    assert flags & qsa.ERROR_FLAGS == 0
+    fids, fsc, fflags = run_select(case, fused=True)
+    assert fflags & qsa.ERROR_FLAGS == 0
+    np.testing.assert_array_equal(fids, ids)
+    rows = np.arange(0, 256, 8)
+    sub = inputs.Case(q=case.q[rows], w=case.w[rows], kblk=case.kblk, n_blocks=case.n_blocks[rows],
+                      tokens=case.tokens[rows], dtype=case.dtype, k=case.k, active_blocks=case.active_blocks)
+    ref = oracle.block_scores(sub.q, sub.w, sub.kblk, sub.n_blocks, sub.dtype)
+    parity.check_rule_b(sc[rows], ref, sub.n_blocks, sub.dtype)
+    parity.check_rule_a(ids[rows], oracle.select_f32(sc[rows], sub.n_blocks, sub.k))
+    parity.check_rule_c(ids[rows], ref, oracle.select(ref, sub.n_blocks, sub.k), sub.n_blocks, sub.k, sub.dtype)
+
+
 @pytest.mark.parametrize("H", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16, inputs.E4M3])
 def test_scorer_heads_and_dtypes(H, dtype):
-    """Every head count, both input types, a group split across CTAs and a ragged tail."""
+    """Every head count, every input type, a group split across CTAs and a ragged tail."""
     nq = 37
     toks = inputs.ragged_tokens(7000 + H, nq, 300)
     case = inputs.make_case(7000 + H + 10 * dtype, nq, H, 300, dtype, toks, 8, active_blocks=300)

@@ -1,5 +1,6 @@
-"""The seeded input generator: bf16 rounding, block counts, determinism."""
+"""The seeded input generator: bf16 and e4m3 rounding, block counts, determinism."""
 import numpy as np
+import pytest
 
 from sparse_attention_kv_gb300 import inputs
 
@@ -42,3 +43,17 @@ def test_named_workloads_shapes_and_determinism():
     r = inputs.stress_case("ragged")
     assert r.n_blocks.min() >= 1 and r.n_blocks.max() <= 2048
     assert (r.tokens % 64 != 0).any()
+
+
+def test_e4m3_rounding_matches_torch_and_breaks_ties_to_even():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32) * s for s in (1e-3, 1.0, 30.0)])
+    mids = ((inputs._E4M3_VALUES[:-1] + inputs._E4M3_VALUES[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids, np.float32([0.0, -0.0, 448.0, -448.0])])
+    ours = inputs.to_e4m3_bits(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours, ref)
+    assert inputs.to_e4m3_bits(np.float32([1e6, -1e6])).tolist() == [0x7E, 0xFE]   # saturated
