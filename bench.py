@@ -16,7 +16,8 @@ ids inside the timed region), SM clocks sampled during the timed region, and
 the CPU oracle timed on a bounded sample of the same workload.  The selection
 attention over the timed call's ids (64 heads in 4 GQA groups of 16, K and V
 caches of 524,288 tokens) is timed beside it, with its own HBM roofline, and
-over the decode window's ids; it is not part of the step.
+over the decode window's ids; it is not part of the step.  So is the deep
+prompt with fp8 e4m3 queries and keys (both select forms and the scorer).
 
 ``--impl reference`` times the CPU oracle (the only reference this method has)
 on the host cores, each step a bounded sample of the same workload.
@@ -456,6 +457,22 @@ def run_ours(args):
     ad_out = torch.empty((adcase.nq, adcase.n_heads, 128), dtype=torch.float32, device=dev)
     ad_lse = torch.empty((adcase.nq, adcase.n_heads), dtype=torch.float32, device=dev)
 
+    # the deep prompt with fp8 e4m3 queries and keys
+    ecase = inputs.deep_e4m3_case()
+    eq, ew, ekb, enb = parity.to_device(ecase, dev)
+    escores = torch.empty((ecase.nq, ecase.max_blocks), dtype=torch.float32, device=dev)
+    eids = torch.empty((ecase.nq, ecase.k), dtype=torch.int32, device=dev)
+    ews = qsa.alloc_workspace(ecase.nq, ecase.max_blocks, ecase.k, fused=True, device=dev)
+
+    def e4m3_chained():
+        qsa.select(eq, ew, ekb, enb, ecase.k, eids, ews, scores=escores, active_blocks=ecase.active_blocks)
+
+    def e4m3_fused():
+        qsa.select(eq, ew, ekb, enb, ecase.k, eids, ews, fused=True, active_blocks=ecase.active_blocks)
+
+    def e4m3_score():
+        qsa.block_scores(eq, ew, ekb, enb, escores, active_blocks=ecase.active_blocks, ws=ews)
+
     def attend():
         qsa.select_attention(*a_dev, a_out, a_lse, scale=acase.scale)
 
@@ -521,6 +538,8 @@ def run_ours(args):
     t_dec_f = timed_loop(torch, decode_fused, reps, flush, stream)
     t_dec_c = timed_loop(torch, decode_chained, reps, flush, stream)
     t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream, prime=False)
+    t_e4m3 = {name: timed_loop(torch, fn, reps, flush, stream)
+              for name, fn in (("chained", e4m3_chained), ("fused", e4m3_fused), ("scorer", e4m3_score))}
     t_attn = timed_loop(torch, attend, 50, flush, stream)
     t_attn_dec = timed_loop(torch, attend_decode, reps, flush, stream)
     # every top-k path forced on the same deep and decode scores (cold), and both select
@@ -587,6 +606,15 @@ def run_ours(args):
     us_e2e = statistics.mean(t_e2e) * 1e3
     attn = attention_report(acase, adcase, statistics.median(t_attn) * 1e3, statistics.median(t_attn_dec) * 1e3,
                             peaks, peak_src)
+    e_us = {k_: statistics.median(v_) * 1e3 for k_, v_ in t_e4m3.items()}
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    e_tf = flops / (e_us["scorer"] * 1e-6) / 1e12
+    e4m3 = {"workload": ecase.name, "select_us": {"chained": e_us["chained"], "fused": e_us["fused"]},
+            "scorer": {"kernel": "scorer_tc_kernel<e4m3, 16>", "bound": "tensor", "us_per_launch": e_us["scorer"],
+                       "achieved": e_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": e_tf / fp8_peak,
+                       "peak_source": f"{peak_src} bf16 burst x 2 (the nominal fp8 / bf16 dense ratio, 4.5 / 2.25)",
+                       "per_launch": f"{flops:.4g} FLOP"},
+            "kblk_bytes": 128.0 * ecase.max_blocks}
     line = {
         "metric": METRIC, "value": us_main, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_main, "higher_is_better": False, "scaling": "weak",
@@ -608,6 +636,7 @@ def run_ours(args):
         "e2e": {"value": us_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "form": form},
         "selection_attention": attn,
+        "e4m3_keys": e4m3,
         "topk_paths_us_cold": topk_paths,
         "warm_back_to_back_us_per_call": warm,
         "gpu_launches": args.steps * (1 if form == "fused" else 1 + topk_launches),
