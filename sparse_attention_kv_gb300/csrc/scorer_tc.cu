@@ -522,12 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int blk = (t_begin + i) * kBM + row;
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * buf_cols);
-            // every column chunk of this thread's part in flight at once, one wait
+            // every column chunk of this thread's part in flight at once, one wait; a
+            // full part (64 columns) in one load, which reads TMEM faster than four
             const int nc = c_end - c_begin;   // <= kMaxChunks
             uint32_t v[kMaxChunks][16];
+            static_assert(kMaxChunks == 4, "one 64-column load per full part");
+            if (nc == kMaxChunks) {
+                tmem_ld64_nowait(taddr + (uint32_t)(c_begin * 16), v);
+            } else {
 #pragma unroll
-            for (int cc = 0; cc < kMaxChunks; ++cc)
-                if (cc < nc) tmem_ld16_nowait(taddr + (uint32_t)((c_begin + cc) * 16), v[cc]);
+                for (int cc = 0; cc < kMaxChunks; ++cc)
+                    if (cc < nc) tmem_ld16_nowait(taddr + (uint32_t)((c_begin + cc) * 16), v[cc]);
+            }
             tmem_wait_ld();
 #pragma unroll
             for (int cc = 0; cc < kMaxChunks; ++cc)
