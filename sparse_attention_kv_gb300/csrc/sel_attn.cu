@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
     }
     __syncthreads();
+    // The kernel may be launched as a programmatic dependent of the one that wrote the
+    // ids (a top-k): nothing the caller wrote is read before this wait.
+    wait_prior_grid();
     if (tid == 0) {   // the group's 16 query rows, two 64-column halves
         mbar_expect_tx(&ct.qfull, 2 * kG * 128);
         for (int hh = 0; hh < 2; ++hh)
@@ -531,23 +534,24 @@ qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
             opted_in[dev] = true;
         }
     }
-    if (ap.split == 1) {
-        sel_attn_kernel<<<grid, kThreads, Bytes, s>>>(mq, mk, mv, ap);
-        return check_cuda(cudaGetLastError(), "sel_attn_kernel launch");
-    }
+    // Always a programmatic dependent: behind a top-k that allows it, the CTAs launch
+    // while the top-k finishes and wait at entry; behind any other work they launch when
+    // it completes, as without the attribute.
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)ap.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)ap.split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return check_cuda(cudaLaunchKernelEx(&cfg, sel_attn_kernel, mq, mk, mv, ap), "sel_attn_kernel cluster launch");
+    cfg.numAttrs = ap.split > 1 ? 2 : 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, sel_attn_kernel, mq, mk, mv, ap), "sel_attn_kernel launch");
 }
 
 }  // namespace

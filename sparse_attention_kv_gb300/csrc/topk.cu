@@ -135,6 +135,7 @@ struct __align__(16) RowSmem {
 template <int R, bool SAMPLE>
 __global__ void __launch_bounds__(kNT, 2) topk_row_kernel(TopkArgs a) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
+    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
     constexpr int KPT = R * 4;
     static_assert(2 * kSampleCap == kRegisterCap, "candidate scores and ids share cand[]");
     __shared__ RowSmem sm;
@@ -251,6 +252,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_row_kernel(TopkArgs a) {
 template <int NT>
 __global__ void __launch_bounds__(NT) topk_radix_kernel(TopkArgs a, int flagged_only) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
+    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
     __shared__ BlockScratch sm;
     const int q = blockIdx.x;
     if (flagged_only && a.qflags[q] == 0u) return;
@@ -337,6 +339,7 @@ struct __align__(16) SplitSmem {
 
 __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chunk_len) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
+    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
     __shared__ SplitSmem sm;
     const int q = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
     const int k = a.k;
@@ -449,6 +452,7 @@ constexpr size_t kWarpTwoPerSmBytes = 90 * 1024;   // dynamic shared memory that
 template <int NW, int CL>
 __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     wait_prior_grid();   // the scores may come from the kernel launched just before
+    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
     __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
     __shared__ __align__(16) uint64_t lists[NW * 32];      // per chunk: its top k, descending
     const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -200,6 +200,32 @@ def test_on_the_ids_of_the_select_path(qsa):
     check_rule_d(out[rows], lse[rows], ref, ref_lse, wabs)
 
 
+@pytest.mark.parametrize("nq,fused", [(3, False), (3, True), (64, False), (64, True)])
+def test_select_then_attention_back_to_back(qsa, nq, fused):
+    """The attention enqueued right behind the select that writes its ids (no host step
+    between, so it launches as the top-k's programmatic dependent)."""
+    sc = inputs.make_case(118 + nq, nq, 16, 2048, inputs.BF16, 131_072, 32, active_blocks=-1 if nq == 3 else 2048)
+    q, w, kb, nb = to_device(sc)
+    c = inputs.make_attention_case(119 + nq, nq, 4, 131_072, sc.tokens, 32)
+    qa, kc, vt, _, nt = attn_to_device(c)
+    ws = qsa.alloc_workspace(nq, 2048, 32, fused=True)
+    ids = torch.full((nq, 32), -9, dtype=torch.int32, device="cuda")
+    scores = None if fused else torch.empty((nq, 2048), dtype=torch.float32, device="cuda")
+    out = torch.full((nq, c.n_heads, 128), float("nan"), device="cuda")
+    lse = torch.full((nq, c.n_heads), float("nan"), device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):   # repeated: every call's attention follows its own select
+        ids.fill_(-9)
+        qsa.select(q, w, kb, nb, 32, ids, ws, scores=scores, fused=fused, active_blocks=sc.active_blocks)
+        qsa.select_attention(qa, kc, vt, ids, nt, out, lse, scale=c.scale, ws=ws)
+    torch.cuda.synchronize()
+    assert qsa.read_flags(ws) & qsa.ERROR_FLAGS == 0
+    c.ids = ids.cpu().numpy()
+    rows = np.arange(nq) if nq <= 8 else np.arange(0, nq, 8)
+    ref, ref_lse, wabs = attention_reference(c, rows)
+    check_rule_d(out.cpu().numpy()[rows], lse.cpu().numpy()[rows], ref, ref_lse, wabs)
+
+
 @pytest.fixture(scope="module")
 def deep_attention():
     """The bench's configuration: 256 queries x 64 heads (4 GQA groups of 16),
