@@ -11,13 +11,13 @@ Functions
 block_scores(q, w, kblk, n_blocks, dtype)
     Double-precision block scores, ``[nq, max_blocks]`` (entries at
     ``b >= n_blocks[q]`` are 0).  ``q``/``kblk`` are float32 arrays, or the bit
-    patterns of bf16 (uint16) or fp8 e4m3 (uint8).
+    patterns of bf16 or fp16 (uint16; fp16 by ``dtype`` only) or fp8 e4m3 (uint8).
 select(scores, n_blocks, k)
     Per-query top-k over double scores: ids ascending, ties to the lower
     block id, -1 padded.
 select_f32(scores, n_blocks, k)
     The same selection over float32 scores (e.g. the GPU's own).
-select_attention(qa, kc, vc, ids, n_tokens, scale)
+select_attention(qa, kc, vc, ids, n_tokens, scale, dtype)
     Selection attention over the selected blocks in double: per query and
     head, softmax(scale * q.K^T) V over the tokens of the query's distinct
     selected blocks below its context length, and the log-sum-exp.  ``qa``
@@ -43,7 +43,8 @@ _lib = None
 F32 = 0
 BF16 = 1
 E4M3 = 2
-_STORAGE = {F32: np.float32, BF16: np.uint16, E4M3: np.uint8}
+F16 = 3
+_STORAGE = {F32: np.float32, BF16: np.uint16, E4M3: np.uint8, F16: np.uint16}
 
 
 def build(force: bool = False) -> str:
@@ -77,7 +78,7 @@ def _load():
         lib.qsa_oracle_select_f32.argtypes = [fp, ctypes.c_int64, i32p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, i32p]
         lib.qsa_oracle_select_f32.restype = ctypes.c_int
-        lib.qsa_oracle_select_attention.argtypes = [vp, vp, vp, i32p, ctypes.c_int, i32p, ctypes.c_int,
+        lib.qsa_oracle_select_attention.argtypes = [vp, vp, vp, ctypes.c_int, i32p, ctypes.c_int, i32p, ctypes.c_int,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_double, dp, dp]
         lib.qsa_oracle_select_attention.restype = ctypes.c_int
@@ -143,8 +144,9 @@ def select_f32(scores: np.ndarray, n_blocks: np.ndarray, k: int) -> np.ndarray:
 
 
 def select_attention(qa: np.ndarray, kc: np.ndarray, vc: np.ndarray, ids: np.ndarray,
-                     n_tokens: np.ndarray, scale: float) -> tuple[np.ndarray, np.ndarray]:
-    """(out [nq,H,D], lse [nq,H]) in double; qa [nq,H,D], kc/vc [Hkv,C,D], ids [nq,k] int32."""
+                     n_tokens: np.ndarray, scale: float, dtype: int = BF16) -> tuple[np.ndarray, np.ndarray]:
+    """(out [nq,H,D], lse [nq,H]) in double; qa [nq,H,D], kc/vc [Hkv,C,D] as bf16 or fp16
+    bits (uint16, ``dtype``), ids [nq,k] int32."""
     lib = _load()
     qa = np.ascontiguousarray(qa, dtype=np.uint16)
     kc = np.ascontiguousarray(kc, dtype=np.uint16)
@@ -158,7 +160,9 @@ def select_attention(qa: np.ndarray, kc: np.ndarray, vc: np.ndarray, ids: np.nda
         raise ValueError("oracle.select_attention: shape mismatch")
     out = np.zeros((nq, H, D), dtype=np.float64)
     lse = np.zeros((nq, H), dtype=np.float64)
-    rc = lib.qsa_oracle_select_attention(qa.ctypes.data, kc.ctypes.data, vc.ctypes.data,
+    if dtype not in (BF16, F16):
+        raise ValueError("oracle.select_attention: bf16 or fp16 inputs")
+    rc = lib.qsa_oracle_select_attention(qa.ctypes.data, kc.ctypes.data, vc.ctypes.data, int(dtype),
                                          _ptr(ids, ctypes.c_int32), int(k), _ptr(n_tokens, ctypes.c_int32),
                                          nq, H, Hkv, D, C, float(scale), _ptr(out, ctypes.c_double),
                                          _ptr(lse, ctypes.c_double))

@@ -40,14 +40,26 @@
 #include <string.h>
 #include <math.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2, ORACLE_F16 = 3 };
 
-/* Widen element i of an fp32, bf16 or fp8 e4m3 array to double, exactly.  e4m3
+/* Widen element i of an fp32, bf16, fp16 or fp8 e4m3 array to double, exactly.  e4m3
  * (the OCP 8-bit floating-point format E4M3): sign, 4 exponent bits with bias
  * 7, 3 mantissa bits; exponent 0 holds the subnormals m x 2^-6 / 8; the pattern
  * with every exponent and mantissa bit set is NaN; there is no infinity. */
 static double widen(const void *base, int dtype, size_t i)
 {
+    if (dtype == ORACLE_F16) {   /* IEEE binary16: 5 exponent bits with bias 15, 10 mantissa bits */
+        uint16_t b = ((const uint16_t *)base)[i];
+        int e = (b >> 10) & 0x1F, m = b & 0x3FF;
+        double v;
+        if (e == 0x1F)
+            v = m ? NAN : INFINITY;
+        else if (e == 0)
+            v = ldexp((double)m, -24);
+        else
+            v = ldexp(1024.0 + m, e - 25);
+        return (b & 0x8000) ? -v : v;
+    }
     if (dtype == ORACLE_E4M3) {
         uint8_t b = ((const uint8_t *)base)[i];
         int e = (b >> 3) & 0xF, m = b & 7;
@@ -88,7 +100,7 @@ int qsa_oracle_block_scores(const void *q, const float *w, const void *kblk, int
 {
     if (!q || !w || !kblk || !n_blocks || !out) return -1;
     if (nq < 0 || n_heads <= 0 || head_dim <= 0 || max_blocks < 0) return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) return -1;
+    if (dtype < ORACLE_F32 || dtype > ORACLE_F16) return -1;
     for (int qi = 0; qi < nq; ++qi) {
         int n = clamp_n(n_blocks[qi], max_blocks);
         for (int b = 0; b < max_blocks; ++b) {
@@ -201,18 +213,19 @@ int qsa_oracle_select_f32(const float *scores, int64_t stride, const int32_t *n_
  *   lse      lse[qi][h] = m + log(sum_t exp(s_t - m))
  *
  * The tokens are visited in slot order; an empty set gives o = 0 and
- * lse = -inf.  Inputs are bf16 bit patterns, widened exactly; everything after
- * that is IEEE double.  qa: [nq][n_heads][head_dim]; kc, vc:
+ * lse = -inf.  Inputs are bf16 or fp16 bit patterns (dtype), widened exactly;
+ * everything after that is IEEE double.  qa: [nq][n_heads][head_dim]; kc, vc:
  * [n_kv_heads][capacity][head_dim] (token rows); ids: [nq][k];
  * out: [nq][n_heads][head_dim]; lse: [nq][n_heads].
  * Returns 0, or -1 on a bad argument.
  */
-int qsa_oracle_select_attention(const uint16_t *qa, const uint16_t *kc, const uint16_t *vc,
+int qsa_oracle_select_attention(const uint16_t *qa, const uint16_t *kc, const uint16_t *vc, int dtype,
                                 const int32_t *ids, int k, const int32_t *n_tokens, int nq,
                                 int n_heads, int n_kv_heads, int head_dim, int capacity,
                                 double scale, double *out, double *lse)
 {
     if (!qa || !kc || !vc || !ids || !n_tokens || !out || !lse) return -1;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
     if (nq < 0 || k <= 0 || n_kv_heads <= 0 || n_heads <= 0 || n_heads % n_kv_heads) return -1;
     if (head_dim <= 0 || capacity < 0) return -1;
     const int group = n_heads / n_kv_heads;
@@ -254,7 +267,7 @@ int qsa_oracle_select_attention(const uint16_t *qa, const uint16_t *kc, const ui
             for (int i = 0; i < n; ++i) {
                 const size_t krow = ((size_t)g * capacity + tok[i]) * head_dim;
                 double dot = 0.0;
-                for (int d = 0; d < head_dim; ++d) dot += widen(qa, ORACLE_BF16, qrow + d) * widen(kc, ORACLE_BF16, krow + d);
+                for (int d = 0; d < head_dim; ++d) dot += widen(qa, dtype, qrow + d) * widen(kc, dtype, krow + d);
                 s[i] = scale * dot;
                 if (s[i] > m) m = s[i];
             }
@@ -263,7 +276,7 @@ int qsa_oracle_select_attention(const uint16_t *qa, const uint16_t *kc, const ui
                 const double e = exp(s[i] - m);
                 const size_t vrow = ((size_t)g * capacity + tok[i]) * head_dim;
                 l += e;
-                for (int d = 0; d < head_dim; ++d) o[d] += e * widen(vc, ORACLE_BF16, vrow + d);
+                for (int d = 0; d < head_dim; ++d) o[d] += e * widen(vc, dtype, vrow + d);
             }
             for (int d = 0; d < head_dim; ++d) o[d] /= l;
             lse[(size_t)qi * n_heads + h] = m + log(l);

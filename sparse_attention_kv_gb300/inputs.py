@@ -77,6 +77,21 @@ def to_e4m3_bits(x: np.ndarray) -> np.ndarray:
     return (idx.astype(np.uint8) | sign).reshape(x.shape)
 
 
+F16 = 3
+
+
+def to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> IEEE binary16 bit patterns (uint16), round to nearest even (numpy's cast)."""
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32).astype(np.float16)).view(np.uint16)
+
+
+def bits_to_f32(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """bf16 or fp16 bit patterns (uint16) -> fp32 values (exact)."""
+    if dtype == F16:
+        return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+    return bf16_bits_to_f32(bits)
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> fp32 values (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
@@ -235,6 +250,7 @@ class AttnCase:
     n_tokens: np.ndarray
     scale: float
     name: str = ""
+    dtype: int = BF16                   # BF16 or F16: the bit patterns' format
 
     @property
     def nq(self) -> int:
@@ -271,8 +287,8 @@ def random_ids(seed: int, n_blocks, k: int, n_valid=None) -> np.ndarray:
     return out
 
 
-def normal_bf16(seed: int, shape, chunks: int = 16) -> np.ndarray:
-    """N(0,1) draws rounded to bf16 bits, in ``chunks`` equal slices of the flat array,
+def normal_bf16(seed: int, shape, chunks: int = 16, dtype: int = BF16) -> np.ndarray:
+    """N(0,1) draws rounded to bf16 (or fp16) bits, in ``chunks`` equal slices of the flat array,
     slice i from the i-th PCG64 stream spawned from ``seed`` (filled in parallel
     threads; the values do not depend on the thread count)."""
     import concurrent.futures as cf
@@ -285,7 +301,8 @@ def normal_bf16(seed: int, shape, chunks: int = 16) -> np.ndarray:
     def fill(i):
         lo, hi = bounds[i]
         g = np.random.Generator(np.random.PCG64(streams[i]))
-        out[lo:hi] = to_bf16_bits(g.standard_normal(hi - lo, dtype=np.float32))
+        draws = g.standard_normal(hi - lo, dtype=np.float32)
+        out[lo:hi] = to_f16_bits(draws) if dtype == F16 else to_bf16_bits(draws)
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(chunks, os.cpu_count() or 1))) as ex:
         list(ex.map(fill, range(chunks)))
@@ -294,19 +311,20 @@ def normal_bf16(seed: int, shape, chunks: int = 16) -> np.ndarray:
 
 def make_attention_case(seed: int, nq: int, n_kv_heads: int, capacity_tokens: int, tokens, k: int, *,
                         group: int = 16, ids: np.ndarray | None = None, n_valid=None,
-                        name: str = "") -> AttnCase:
-    """qa, kc, vc ~ N(0,1) (bf16), contexts ``tokens`` (scalar or per query); the
-    ids are random distinct blocks of each context unless given."""
+                        name: str = "", dtype: int = BF16) -> AttnCase:
+    """qa, kc, vc ~ N(0,1) (bf16, or fp16 with dtype F16), contexts ``tokens`` (scalar
+    or per query); the ids are random distinct blocks of each context unless given."""
     rng = np.random.default_rng(seed)
     H = n_kv_heads * group
-    qa = to_bf16_bits(rng.standard_normal((nq, H, HEAD_DIM), dtype=np.float32))
-    kc = normal_bf16(seed + 2, (n_kv_heads, capacity_tokens, HEAD_DIM))
-    vc = normal_bf16(seed + 3, (n_kv_heads, capacity_tokens, HEAD_DIM))
+    draws = rng.standard_normal((nq, H, HEAD_DIM), dtype=np.float32)
+    qa = to_f16_bits(draws) if dtype == F16 else to_bf16_bits(draws)
+    kc = normal_bf16(seed + 2, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
+    vc = normal_bf16(seed + 3, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
     toks = np.broadcast_to(np.asarray(tokens, dtype=np.int64), (nq,)).astype(np.int32)
     if ids is None:
         ids = random_ids(seed + 1, blocks_for_tokens(toks), k, n_valid)
     return AttnCase(qa=qa, kc=kc, vc=vc, ids=np.ascontiguousarray(ids, dtype=np.int32), n_tokens=toks,
-                    scale=HEAD_DIM ** -0.5, name=name)
+                    scale=HEAD_DIM ** -0.5, name=name, dtype=dtype)
 
 
 ATTN_KV_HEADS = 4

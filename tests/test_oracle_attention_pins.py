@@ -22,13 +22,17 @@ from sparse_attention_kv_gb300 import inputs
 bf16 = inputs.to_bf16_bits
 
 
-def _attn(qa, kc, vc, ids, n_tokens, scale):
-    return oracle.select_attention(bf16(np.asarray(qa, np.float32)), bf16(np.asarray(kc, np.float32)),
-                                   bf16(np.asarray(vc, np.float32)), np.asarray(ids, np.int32),
-                                   np.asarray(n_tokens, np.int32), scale)
+def _bits(x, dtype):
+    x = np.asarray(x, np.float32)
+    return inputs.to_f16_bits(x) if dtype == oracle.F16 else bf16(x)
 
 
-def test_two_tokens_closed_form():
+def _attn(qa, kc, vc, ids, n_tokens, scale, dtype=oracle.BF16):
+    return oracle.select_attention(_bits(qa, dtype), _bits(kc, dtype), _bits(vc, dtype), np.asarray(ids, np.int32),
+                                   np.asarray(n_tokens, np.int32), scale, dtype)
+
+
+def test_two_tokens_closed_form(dtype=oracle.BF16):
     # block 1 of a 66-token context holds tokens 64 and 65; every other row would
     # dominate (or stand out) if it leaked in
     kc = np.full((1, 128, 2), 8.0, np.float32)
@@ -37,7 +41,7 @@ def test_two_tokens_closed_form():
     kc[0, 64], kc[0, 65] = (1.0, 0.0), (0.0, 1.0)
     vc[0, 64], vc[0, 65] = (1.0, 2.0), (3.0, 4.0)
     qa = np.array([[[1.0, 0.0], [0.0, 2.0]]], np.float32)
-    out, lse = _attn(qa, kc, vc, [[1, -1]], [66], 0.5)
+    out, lse = _attn(qa, kc, vc, [[1, -1]], [66], 0.5, dtype)
     e = math.exp(0.5)
     a0, b0 = e / (e + 1), 1 / (e + 1)                       # head 0: logits 0.5, 0
     a1, b1 = 1 / (1 + math.e), math.e / (1 + math.e)        # head 1: logits 0, 1
@@ -78,19 +82,19 @@ def test_equal_keys_give_the_mean_of_values():
     assert (np.abs(lse[0] - lse[1] - (math.log(192) - math.log(86))) < 1e-12).all()
 
 
-def test_every_block_selected_is_dense_causal_attention():
+def test_every_block_selected_is_dense_causal_attention(dtype=oracle.BF16):
     torch = pytest.importorskip("torch")
     import torch.nn.functional as F
     n_tokens = [300, 64, 257, 1]
-    c = inputs.make_attention_case(73, 4, 2, 320, n_tokens, 5, group=3)
+    c = inputs.make_attention_case(73, 4, 2, 320, n_tokens, 5, group=3, dtype=dtype)
     nb = inputs.blocks_for_tokens(c.n_tokens)
     ids = np.full((4, 5), -1, np.int32)
     for q in range(4):
         ids[q, :nb[q]] = np.arange(nb[q])
-    out, lse = oracle.select_attention(c.qa, c.kc, c.vc, ids, c.n_tokens, c.scale)
-    qf = torch.from_numpy(inputs.bf16_bits_to_f32(c.qa).astype(np.float64))
-    kf = torch.from_numpy(inputs.bf16_bits_to_f32(c.kc).astype(np.float64))
-    vf = torch.from_numpy(inputs.bf16_bits_to_f32(c.vc).astype(np.float64))
+    out, lse = oracle.select_attention(c.qa, c.kc, c.vc, ids, c.n_tokens, c.scale, dtype)
+    qf = torch.from_numpy(inputs.bits_to_f32(c.qa, dtype).astype(np.float64))
+    kf = torch.from_numpy(inputs.bits_to_f32(c.kc, dtype).astype(np.float64))
+    vf = torch.from_numpy(inputs.bits_to_f32(c.vc, dtype).astype(np.float64))
     for q in range(4):
         n = n_tokens[q]
         for h in range(c.n_heads):
@@ -100,6 +104,14 @@ def test_every_block_selected_is_dense_causal_attention():
             np.testing.assert_allclose(out[q, h], ref.numpy(), rtol=1e-11, atol=1e-12)
             ref_lse = torch.logsumexp(c.scale * (kf[g, :n] @ qf[q, h]), 0).item()
             assert abs(lse[q, h] - ref_lse) < 1e-11
+
+
+def test_two_tokens_closed_form_f16():
+    test_two_tokens_closed_form(oracle.F16)
+
+
+def test_every_block_selected_is_dense_causal_attention_f16():
+    test_every_block_selected_is_dense_causal_attention(oracle.F16)
 
 
 def test_slot_order_pads_and_duplicates_do_not_matter():
@@ -175,7 +187,7 @@ MUTANTS = {
     "no_max_shift": ("const double e = exp(s[i] - m);", "const double e = exp(s[i]);"),
     "lse_without_max": ("lse[(size_t)qi * n_heads + h] = m + log(l);", "lse[(size_t)qi * n_heads + h] = log(l);"),
     "no_dedup": ("if (seen) continue;", ""),
-    "values_from_keys": ("o[d] += e * widen(vc, ORACLE_BF16, vrow + d);", "o[d] += e * widen(kc, ORACLE_BF16, vrow + d);"),
+    "values_from_keys": ("o[d] += e * widen(vc, dtype, vrow + d);", "o[d] += e * widen(kc, dtype, vrow + d);"),
     "transposed_q_index": ("const size_t qrow = ((size_t)qi * n_heads + h) * head_dim;",
                            "const size_t qrow = ((size_t)h * nq + qi) * head_dim;"),
     "no_normalise": ("for (int d = 0; d < head_dim; ++d) o[d] /= l;", ""),

@@ -141,6 +141,32 @@ def test_e4m3_widening_matches_torch_for_every_finite_code():
     np.testing.assert_array_equal(_e4m3_values(codes), ref)
 
 
+def _f16_values(codes):
+    """Values of fp16 codes read through the scorer (as _e4m3_values)."""
+    kb = np.zeros((len(codes), 128), dtype=np.uint16)
+    kb[:, 0] = codes
+    n = np.array([len(codes)], np.int32)
+    w = np.ones((1, 1), np.float32)
+    pos, neg = np.zeros((1, 1, 128), np.uint16), np.zeros((1, 1, 128), np.uint16)
+    pos[0, 0, 0], neg[0, 0, 0] = 0x3C00, 0xBC00            # +1.0 and -1.0
+    return oracle.block_scores(pos, w, kb, n, oracle.F16)[0] - oracle.block_scores(neg, w, kb, n, oracle.F16)[0]
+
+
+def test_f16_widening_spec_values():
+    # IEEE 754 binary16: bias 15; largest finite 0x7BFF = 65504, smallest normal 0x0400 =
+    # 2^-14, smallest subnormal 0x0001 = 2^-24, largest subnormal 0x03FF, 1.0 = 0x3C00
+    codes = [0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x3C00, 0x3E00, 0x4000, 0x7BFF, 0xFBFF, 0xC000, 0x3555]
+    want = [0.0, 0.0, 2.0 ** -24, 1023 * 2.0 ** -24, 2.0 ** -14, 1.0, 1.5, 2.0, 65504.0, -65504.0, -2.0,
+            (1024 + 0x155) * 2.0 ** (13 - 25)]
+    np.testing.assert_array_equal(_f16_values(codes), want)
+
+
+def test_f16_widening_matches_numpy_for_every_finite_code():
+    codes = np.arange(1 << 16, dtype=np.uint32)
+    codes = codes[((codes >> 10) & 0x1F) != 0x1F].astype(np.uint16)      # drop infinities and NaNs
+    np.testing.assert_array_equal(_f16_values(codes), codes.view(np.float16).astype(np.float64))
+
+
 def test_bf16_matches_widened_fp32():
     """Scores of bf16 bits equal the scores of their exact fp32 widening."""
     c = inputs.make_case(21, 2, 4, 30, inputs.BF16, 30 * 64, 8)
@@ -287,6 +313,9 @@ MUTANTS = {
     "e4m3_bias": ("v = ldexp(8.0 + m, e - 10);", "v = ldexp(8.0 + m, e - 9);"),
     "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     "e4m3_sign": ("return (b & 0x80) ? -v : v;", "return v;"),
+    "f16_bias": ("v = ldexp(1024.0 + m, e - 25);", "v = ldexp(1024.0 + m, e - 24);"),
+    "f16_subnormal": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "f16_sign": ("return (b & 0x8000) ? -v : v;", "return v;"),
 }
 
 
@@ -297,7 +326,8 @@ def test_pins_catch_planted_oracle_mistakes(tmp_path, golden_dir, monkeypatch):
     pins = [test_scores_hand_fixture, test_bf16_widening_fixture, test_relu_per_head_identities,
             test_exactly_rounded_sum_crosscheck, test_select_hand_fixture,
             test_select_brute_force_tiny, test_select_closed_forms,
-            test_select_64_levels_lowest_ids_on_boundary_level, test_e4m3_widening_spec_values]
+            test_select_64_levels_lowest_ids_on_boundary_level, test_e4m3_widening_spec_values,
+            test_f16_widening_spec_values]
     for name, (old, new) in MUTANTS.items():
         assert old in src, name
         msrc = tmp_path / f"{name}.c"
