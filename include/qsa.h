@@ -63,8 +63,9 @@ typedef enum {
 typedef enum {
     QSA_F32 = 0,  /* IEEE binary32 */
     QSA_BF16 = 1, /* bfloat16 (upper half of a binary32) */
-    QSA_E4M3 = 2  /* 8-bit floating point E4M3 of the OCP FP8 specification (sign, 4 exponent bits
+    QSA_E4M3 = 2, /* 8-bit floating point E4M3 of the OCP FP8 specification (sign, 4 exponent bits
                      with bias 7, 3 mantissa bits; no infinities, S.1111.111 = NaN) */
+    QSA_F16 = 3   /* IEEE binary16 (qsa_select_attention only) */
 } qsa_dtype;
 
 /* Top-k path.  AUTO picks from host-visible sizes only; the others force a path
@@ -220,9 +221,10 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
  * ids[q][0..k) with t < n_tokens[q].  A query with no such token gets o = 0 and
  * lse = -inf.
  *
- *   qa        [nq][n_heads][128] bf16, row-major, 16-byte aligned
- *   kcache    [n_kv_heads][capacity][128] bf16 (K[g][t] = token rows), 16-byte aligned
- *   vcache_t  [n_kv_heads][capacity / 64][128][64] bf16: each 64-token block of V
+ *   dt        QSA_BF16 or QSA_F16: the format of qa, kcache and vcache_t
+ *   qa        [nq][n_heads][128] dtype `dt`, row-major, 16-byte aligned
+ *   kcache    [n_kv_heads][capacity][128] dtype `dt` (K[g][t] = token rows), 16-byte aligned
+ *   vcache_t  [n_kv_heads][capacity / 64][128][64] dtype `dt`: each 64-token block of V
  *             stored dimension-major, element [g][b][d][r] = V[g][64 b + r][d];
  *             16-byte aligned
  *   ids       [nq][k] int32: block ids (e.g. the ids of qsa_select), -1 = none, in
@@ -236,17 +238,20 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
  *   ws        a workspace of at least 256 bytes (its flags word is used), or NULL
  *             (then device flags are not recorded)
  *
- * Arithmetic: the q.k products on the tensor cores (bf16 x bf16 -> fp32); the
- * weights exp2((s - m) scale log2 e) in fp32, rounded to bf16 for the P.V product
- * on the tensor cores (bf16 x bf16 -> fp32), and divided by the sum of the
- * rounded weights.  Tokens at or past n_tokens take no part, whatever their K and
- * V rows hold.
+ * Arithmetic: the q.k products on the tensor cores (16-bit x 16-bit -> fp32); the
+ * weights exp2((s - m) scale log2 e) in fp32, rounded to `dt` for the P.V product
+ * on the tensor cores (-> fp32), and divided by the sum of the rounded weights.
+ * Tokens at or past n_tokens take no part, whatever their K and V rows hold.
+ * Launch: the kernel is launched as a programmatic dependent of the work before it
+ * on `stream`; it reads nothing the caller wrote until that work has completed, so
+ * behind a top-k of this library it starts while the top-k finishes.
  * Errors: QSA_ERR_INVALID_ARG for NULL qa/kcache/vcache_t/ids/n_tokens/out,
  * nq < 1, head_dim != 128, n_kv_heads < 1, n_heads != QSA_ATTN_GROUP *
  * n_kv_heads, k outside [1, QSA_ATTN_MAX_K], capacity < 64 or not a multiple of
  * 64, n_kv_heads * capacity >= 2^30, nq * n_heads >= 2^30, misaligned
  * qa/kcache/vcache_t, scale not finite or <= 0, ws smaller than 256 bytes or
- * not 256-byte aligned; QSA_ERR_UNSUPPORTED for a dtype other than QSA_BF16.
+ * not 256-byte aligned; QSA_ERR_UNSUPPORTED for a dtype other than QSA_BF16 or
+ * QSA_F16.
  */
 qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *vcache_t, qsa_dtype dt,
                                 const int32_t *ids, int k, const int32_t *n_tokens, int nq, int n_heads,

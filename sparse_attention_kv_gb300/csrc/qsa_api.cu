@@ -310,8 +310,10 @@ qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *
     if (!(scale > 0.0f) || !(scale <= 3.4e38f)) return fail(QSA_ERR_INVALID_ARG, "scale must be finite and > 0");
     if (ws && (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return fail(QSA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold at least 256 bytes");
-    if (dt != QSA_BF16) return fail(QSA_ERR_UNSUPPORTED, "selection attention takes bf16 inputs only (dtype %d)", dt);
+    if (dt != QSA_BF16 && dt != QSA_F16)
+        return fail(QSA_ERR_UNSUPPORTED, "selection attention takes bf16 or fp16 inputs (dtype %d)", dt);
     AttnArgs a{};
+    a.dt = dt;
     a.qa = qa;
     a.kcache = kcache;
     a.vcache_t = vcache_t;

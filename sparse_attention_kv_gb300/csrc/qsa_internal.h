@@ -19,7 +19,8 @@ qsa_status check_cuda(cudaError_t err, const char *what);
 int num_sms();  // SM count of the current device (cached per device)
 
 // A 2-D TMA tensor map over a row-major [rows][inner] array of esize-byte elements
-// (4: fp32, 2: bf16, 1: 8-bit), box of 128 bytes x box_rows, 128-byte swizzle;
+// (4: fp32, 2: bf16 or fp16, 1: 8-bit; the bytes are copied as they are), box of
+// 128 bytes x box_rows, 128-byte swizzle;
 // encoded once per (pointer, shape, device).
 qsa_status get_map(CUtensorMap *out, const void *ptr, int esize, uint32_t inner, uint64_t rows, uint32_t box_rows);
 
@@ -103,6 +104,7 @@ struct ScorerArgs {
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);
 
 struct AttnArgs {
+    qsa_dtype dt;   // QSA_BF16 or QSA_F16
     const void *qa;
     const void *kcache;
     const void *vcache_t;

@@ -25,7 +25,8 @@
 //      logit tile, which is consumed first.
 // The V cache holds every 64-token block dimension-major ([128][64]), so both
 // operands of both products are K-major under the 128-byte swizzle that TMA
-// writes.  Warp 0 issues TMA loads (K pairs, then V pairs, through one ring),
+// writes (q, K and V in bf16 or fp16; the weights in the same format).  Warp 0
+// issues TMA loads (K pairs, then V pairs, through one ring),
 // warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax and the
 // epilogue.
 //
@@ -41,6 +42,7 @@
 // its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <mutex>
@@ -60,7 +62,8 @@ constexpr int kPStages = 2;             // P ring stages
 constexpr int kPBytes = 4096;           // two blocks x 16 heads x 64 tokens bf16
 constexpr int kThreads = 192;           // TMA warp, MMA warp, four softmax warps
 constexpr int kSoft = 128;
-constexpr uint32_t kFmtBF16 = 1;
+// instruction-descriptor A/B formats of kind::f16
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1;
 
 constexpr int kOffQ = 0;                                  // 2 halves x 16 rows x 128 B
 constexpr int kOffKV = 4096;
@@ -159,6 +162,22 @@ __device__ __forceinline__ void clear_tail(uint8_t *blk, int r) {
         }
 }
 
+// The weights of the P.V product in the inputs' 16-bit format, and their value.
+template <bool F16>
+__device__ __forceinline__ float store_weight(uint8_t *dst, float e) {
+    if constexpr (F16) {
+        const __half eh = __float2half_rn(e);
+        *reinterpret_cast<__half *>(dst) = eh;
+        return __half2float(eh);
+    } else {
+        const __nv_bfloat16 eb = __float2bfloat16_rn(e);
+        *reinterpret_cast<__nv_bfloat16 *>(dst) = eb;
+        return __bfloat162float(eb);
+    }
+}
+
+// F16: q, K and V (and so the weights) are fp16; otherwise bf16.
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     sel_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -314,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            const uint32_t id = idesc(kFmtBF16, 128, kG);
+            const uint32_t id = idesc(F16 ? kFmtF16 : kFmtBF16, 128, kG);
             bool ok = mbar_wait(&ct.qfull, 0, abort_flag);
             tc_fence_after();
             const uint32_t q0 = smem_u32(sQ);
@@ -417,9 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < kG; ++h) {
                     const float e = vis ? exp2f(fmaf(__uint_as_float(v[h]), p.scale_log2, -mc[h])) : 0.0f;
-                    const __nv_bfloat16 eb = __float2bfloat16_rn(e);
-                    l[h] += __bfloat162float(eb);
-                    *reinterpret_cast<__nv_bfloat16 *>(pb + swz(h, tok)) = eb;
+                    l[h] += store_weight<F16>(pb + swz(h, tok), e);
                 }
             }
             fence_proxy_async();   // the weights are read by the tensor core
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int Bytes>
+template <int Bytes, bool F16>
 qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &ap,
                        int grid, cudaStream_t s) {
     static std::mutex mu;
@@ -527,7 +544,7 @@ qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!opted_in[dev]) {
-            st = check_cuda(cudaFuncSetAttribute(sel_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            st = check_cuda(cudaFuncSetAttribute(sel_attn_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  kSmemOneBytes),
                             "cudaFuncSetAttribute(selection attention)");
             if (st != QSA_OK) return st;
@@ -551,7 +568,7 @@ qsa_status launch_with(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = ap.split > 1 ? 2 : 1;
-    return check_cuda(cudaLaunchKernelEx(&cfg, sel_attn_kernel, mq, mk, mv, ap), "sel_attn_kernel launch");
+    return check_cuda(cudaLaunchKernelEx(&cfg, sel_attn_kernel<F16>, mq, mk, mv, ap), "sel_attn_kernel launch");
 }
 
 }  // namespace
@@ -588,8 +605,12 @@ qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s) {
         ap.split *= 2;
     const int grid = units * ap.split;
     // more than 32 blocks in one CTA can take all 512 TMEM columns: one CTA per SM
-    return a.k > 32 && ap.split == 1 ? launch_with<kSmemOneBytes>(mq, mk, mv, ap, grid, s)
-                                     : launch_with<kSmemBytes>(mq, mk, mv, ap, grid, s);
+    const bool alone = a.k > 32 && ap.split == 1;
+    if (a.dt == QSA_F16)
+        return alone ? launch_with<kSmemOneBytes, true>(mq, mk, mv, ap, grid, s)
+                     : launch_with<kSmemBytes, true>(mq, mk, mv, ap, grid, s);
+    return alone ? launch_with<kSmemOneBytes, false>(mq, mk, mv, ap, grid, s)
+                 : launch_with<kSmemBytes, false>(mq, mk, mv, ap, grid, s);
 }
 
 }  // namespace qsa

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libqsa.so")
 # qsa_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 # qsa_dtype
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, F16 = 0, 1, 2, 3
 # qsa_path
 PATH_AUTO, PATH_SPLIT, PATH_SAMPLE, PATH_REGISTER, PATH_RADIX, PATH_WARP = range(6)
 PATH_NAMES = {PATH_AUTO: "auto", PATH_SPLIT: "split", PATH_SAMPLE: "sample",
@@ -225,14 +225,14 @@ def select_attention(qa: torch.Tensor, kcache: torch.Tensor, vcache_t: torch.Ten
                      scale: float | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Selection attention over ids [nq, k]: out [nq, H, 128] fp32 (and lse [nq, H]).
 
-    qa [nq, H, 128] bf16, kcache [Hkv, C, 128] bf16, vcache_t [Hkv, C/64, 128, 64] bf16
-    (each block of V dimension-major), n_tokens [nq] int32; H = 16 * Hkv."""
+    qa [nq, H, 128], kcache [Hkv, C, 128], vcache_t [Hkv, C/64, 128, 64] (each block of V
+    dimension-major), all bfloat16 or all float16; n_tokens [nq] int32; H = 16 * Hkv."""
     lib = load()
     for t, nm in ((qa, "qa"), (kcache, "kcache"), (vcache_t, "vcache_t"), (ids, "ids"), (n_tokens, "n_tokens"),
                   (out, "out")):
         _contig(t, nm)
-    if qa.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16 or vcache_t.dtype != torch.bfloat16:
-        raise ValueError("qa, kcache and vcache_t must be bfloat16")
+    if qa.dtype not in (torch.bfloat16, torch.float16) or kcache.dtype != qa.dtype or vcache_t.dtype != qa.dtype:
+        raise ValueError("qa, kcache and vcache_t must all be bfloat16 or all float16")
     if ids.dtype != torch.int32 or n_tokens.dtype != torch.int32:
         raise ValueError("ids and n_tokens must be int32")
     nq, H, D = qa.shape
@@ -245,7 +245,8 @@ def select_attention(qa: torch.Tensor, kcache: torch.Tensor, vcache_t: torch.Ten
         raise ValueError("lse must be a contiguous fp32 tensor [nq, n_heads]")
     if scale is None:
         scale = D ** -0.5
-    st = lib.qsa_select_attention(_dptr(qa, "qa"), _dptr(kcache, "kcache"), _dptr(vcache_t, "vcache_t"), BF16,
+    st = lib.qsa_select_attention(_dptr(qa, "qa"), _dptr(kcache, "kcache"), _dptr(vcache_t, "vcache_t"),
+                                  F16 if qa.dtype == torch.float16 else BF16,
                                   _dptr(ids, "ids"), ids.shape[1], _dptr(n_tokens, "n_tokens"), nq, H, Hkv, D, C,
                                   float(scale), _dptr(out, "out"), _dptr(lse, "lse"), _dptr(ws, "ws"),
                                   0 if ws is None else ws.numel(), _stream(stream))

@@ -118,6 +118,7 @@ def test_select_rejects_bad_arguments_before_launch(lib, case, status):
     (dict(ws=FAKE + 64), qsa.ERR_WORKSPACE),
     (dict(dt=qsa.F32), qsa.ERR_UNSUPPORTED),
     (dict(dt=qsa.E4M3), qsa.ERR_UNSUPPORTED),
+    (dict(dt=9), qsa.ERR_UNSUPPORTED),
 ])
 def test_select_attention_rejects_bad_arguments_before_launch(lib, case, status):
     a = dict(qa=FAKE, kcache=FAKE, vcache=FAKE, dt=qsa.BF16, ids=FAKE, k=32, n_tokens=FAKE, nq=4, n_heads=64,

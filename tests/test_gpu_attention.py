@@ -1,6 +1,6 @@
 """Selection attention on the GPU against the FP64 oracle (parity rule (d)).
 
-Small cases span several pair tiles, odd block counts, pads, ragged contexts
+Small cases (bf16 and fp16) span several pair tiles, odd block counts, pads, ragged contexts
 with partial tail blocks, k = 1 .. 64 (the one-CTA-per-SM form above 32), one
 unit per CTA and units split over clusters, grids of more CTAs than the GPU holds,
 several GQA groups, unsorted and repeated ids, ids past the context, NaN in the
@@ -59,21 +59,22 @@ CASES = [
 ]
 
 
-def _case(seed, nq, n_kv, cap, tokens, k, n_valid):
+def _case(seed, nq, n_kv, cap, tokens, k, n_valid, dtype=inputs.BF16):
     if tokens == "ragged":
         tokens = inputs.ragged_tokens(seed, nq, cap // 64)
     if n_valid == "random":
         n_valid = np.random.default_rng(seed).integers(0, k + 1, size=nq)
-    return inputs.make_attention_case(seed, nq, n_kv, cap, tokens, k, n_valid=n_valid)
+    return inputs.make_attention_case(seed, nq, n_kv, cap, tokens, k, n_valid=n_valid, dtype=dtype)
 
 
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F16], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("params", CASES, ids=[f"nq{c[1]}-kv{c[2]}-C{c[3]}-{c[4]}-k{c[5]}" for c in CASES])
-def test_matches_oracle(qsa, params):
-    c = _case(*params)
+def test_matches_oracle(qsa, params, dtype):
+    c = _case(*params, dtype=dtype)
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
-    ref, ref_lse, wabs = attention_reference(c)
-    check_rule_d(out, lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, bounds)
     assert qsa.read_flags(ws) == 0
 
 
@@ -90,8 +91,8 @@ def test_more_units_than_resident_ctas_match_oracle(qsa, params):
     c = _case(*params)
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
-    ref, ref_lse, wabs = attention_reference(c)
-    check_rule_d(out, lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, bounds)
     assert qsa.read_flags(ws) == 0
 
 
@@ -104,9 +105,9 @@ def test_split_and_unsplit_forms_both_match(qsa):
     sub = inputs.AttnCase(qa=c.qa[rows], kc=c.kc, vc=c.vc, ids=c.ids[rows], n_tokens=c.n_tokens[rows],
                           scale=c.scale)
     part, part_lse = _run(qsa, sub)
-    ref, ref_lse, wabs = attention_reference(c, rows)
-    check_rule_d(full[rows], full_lse[rows], ref, ref_lse, wabs)
-    check_rule_d(part, part_lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c, rows)
+    check_rule_d(full[rows], full_lse[rows], ref, ref_lse, bounds)
+    check_rule_d(part, part_lse, ref, ref_lse, bounds)
     assert not np.array_equal(part, full[rows])   # two different reductions
 
 
@@ -130,21 +131,22 @@ def test_unsorted_repeated_and_out_of_context_ids(qsa):
     c.ids = ids
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
-    ref, ref_lse, wabs = attention_reference(c)
-    check_rule_d(out, lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, bounds)
     assert qsa.read_flags(ws) == qsa.FLAG_BAD_ID
 
 
-def test_cache_rows_past_the_context_take_no_part(qsa):
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F16], ids=["bf16", "fp16"])
+def test_cache_rows_past_the_context_take_no_part(qsa, dtype):
     """NaN in every K and V row at or past each query's context: outputs unchanged, bit for bit."""
     n = 64 * 37 + 23                                   # a partial tail block
-    c = inputs.make_attention_case(112, 8, 1, 4096, n, 32)
+    c = inputs.make_attention_case(112, 8, 1, 4096, n, 32, dtype=dtype)
     base = inputs.random_ids(113, np.full(8, 37), 31)
     for q in range(8):                                 # 31 blocks below the tail, then the tail block
         v = base[q][base[q] >= 0]
         c.ids[q] = np.r_[v, 37, np.full(31 - len(v), -1)]
     clean, clean_lse = _run(qsa, c)
-    nan = np.uint16(0x7FC0)
+    nan = np.uint16(0x7E00 if dtype == inputs.F16 else 0x7FC0)
     c.kc = c.kc.copy()
     c.vc = c.vc.copy()
     c.kc[:, n:] = nan
@@ -152,8 +154,8 @@ def test_cache_rows_past_the_context_take_no_part(qsa):
     dirty, dirty_lse = _run(qsa, c)
     np.testing.assert_array_equal(dirty, clean)
     np.testing.assert_array_equal(dirty_lse, clean_lse)
-    ref, ref_lse, wabs = attention_reference(c)
-    check_rule_d(dirty, dirty_lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c)
+    check_rule_d(dirty, dirty_lse, ref, ref_lse, bounds)
 
 
 def test_empty_token_sets(qsa):
@@ -164,9 +166,9 @@ def test_empty_token_sets(qsa):
     c.ids[2, 0] = 31                  # in context
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
-    ref, ref_lse, wabs = attention_reference(c)
+    ref, ref_lse, bounds = attention_reference(c)
     assert np.isneginf(ref_lse[:2]).all()
-    check_rule_d(out, lse, ref, ref_lse, wabs)
+    check_rule_d(out, lse, ref, ref_lse, bounds)
     assert qsa.read_flags(ws) == qsa.FLAG_BAD_ID
 
 
@@ -176,8 +178,8 @@ def test_context_past_capacity_is_clamped(qsa):
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
     c.n_tokens[2] = 2048
-    ref, ref_lse, wabs = attention_reference(c)
-    check_rule_d(out, lse, ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c)
+    check_rule_d(out, lse, ref, ref_lse, bounds)
     assert qsa.read_flags(ws) == qsa.FLAG_NBLOCKS_CLAMPED
 
 
@@ -196,8 +198,8 @@ def test_on_the_ids_of_the_select_path(qsa):
     c = inputs.make_attention_case(117, 64, 4, 131_072, sc.tokens, 32, ids=ids)
     out, lse = _run(qsa, c, ids=ids_c)
     rows = np.arange(0, 64, 4)
-    ref, ref_lse, wabs = attention_reference(c, rows)
-    check_rule_d(out[rows], lse[rows], ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c, rows)
+    check_rule_d(out[rows], lse[rows], ref, ref_lse, bounds)
 
 
 @pytest.mark.parametrize("nq,fused", [(3, False), (3, True), (64, False), (64, True)])
@@ -222,8 +224,8 @@ def test_select_then_attention_back_to_back(qsa, nq, fused):
     assert qsa.read_flags(ws) & qsa.ERROR_FLAGS == 0
     c.ids = ids.cpu().numpy()
     rows = np.arange(nq) if nq <= 8 else np.arange(0, nq, 8)
-    ref, ref_lse, wabs = attention_reference(c, rows)
-    check_rule_d(out.cpu().numpy()[rows], lse.cpu().numpy()[rows], ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c, rows)
+    check_rule_d(out.cpu().numpy()[rows], lse.cpu().numpy()[rows], ref, ref_lse, bounds)
 
 
 @pytest.fixture(scope="module")
@@ -238,7 +240,7 @@ def test_deep_prompt_sampled_queries(qsa, deep_attention):
     ws = _ws(qsa)
     out, lse = _run(qsa, c, ws)
     rows = np.array([0, 1, 77, 128, 200, 255])
-    ref, ref_lse, wabs = attention_reference(c, rows)
-    check_rule_d(out[rows], lse[rows], ref, ref_lse, wabs)
+    ref, ref_lse, bounds = attention_reference(c, rows)
+    check_rule_d(out[rows], lse[rows], ref, ref_lse, bounds)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     assert qsa.read_flags(ws) == 0
