@@ -18,17 +18,19 @@
 //      logits stay in TMEM (k <= 64 blocks -> at most 512 columns).
 //   2. Four softmax warps (one TMEM lane = one token each) take the per-head
 //      maximum over every visible token, then write p = exp2((s - m) * scale *
-//      log2 e) rounded to bf16 into a shared-memory ring and sum the rounded
-//      values, so the output is an exact convex combination of the weights used.
+//      log2 e) rounded to the inputs' 16-bit format into a shared-memory ring and
+//      sum the rounded values, so the output is an exact convex combination of
+//      the weights used.
 //   3. O^T += V_b^T . P_b^T on tcgen05 (M = 128 head dims, N = 16 heads, K = 64
 //      tokens per block) accumulates in TMEM over the columns of the first
 //      logit tile, which is consumed first.
 // The V cache holds every 64-token block dimension-major ([128][64]), so both
 // operands of both products are K-major under the 128-byte swizzle that TMA
 // writes (q, K and V in bf16 or fp16; the weights in the same format).  Warp 0
-// issues TMA loads (K pairs, then V pairs, through one ring),
-// warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax and the
-// epilogue.
+// issues TMA loads (K pairs, then V pairs, through one ring), warp 1 owns TMEM
+// and issues the MMAs, warps 2-5 run the softmax and the epilogue.  The kernel
+// is launched as a programmatic dependent of the work before it and reads
+// nothing the caller wrote until that work has completed.
 //
 // When the (query, KV head) units are too few to fill the GPU (a decode
 // window), each unit's pairs are split over a thread-block cluster of 2, 4 or 8
