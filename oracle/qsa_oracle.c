@@ -48,18 +48,14 @@ enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2, ORACLE_F16 = 3 };
  * with every exponent and mantissa bit set is NaN; there is no infinity. */
 static double widen(const void *base, int dtype, size_t i)
 {
-    if (dtype == ORACLE_F16) {   /* IEEE binary16: 5 exponent bits with bias 15, 10 mantissa bits */
-        uint16_t b = ((const uint16_t *)base)[i];
-        int e = (b >> 10) & 0x1F, m = b & 0x3FF;
-        double v;
-        if (e == 0x1F)
-            v = m ? NAN : INFINITY;
-        else if (e == 0)
-            v = ldexp((double)m, -24);
-        else
-            v = ldexp(1024.0 + m, e - 25);
-        return (b & 0x8000) ? -v : v;
+    if (dtype == ORACLE_BF16) {   /* the upper half of a binary32 */
+        uint16_t h = ((const uint16_t *)base)[i];
+        uint32_t u = ((uint32_t)h) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        return (double)f;
     }
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[i];
     if (dtype == ORACLE_E4M3) {
         uint8_t b = ((const uint8_t *)base)[i];
         int e = (b >> 3) & 0xF, m = b & 7;
@@ -72,14 +68,17 @@ static double widen(const void *base, int dtype, size_t i)
             v = ldexp(8.0 + m, e - 10);
         return (b & 0x80) ? -v : v;
     }
-    if (dtype == ORACLE_BF16) {
-        uint16_t h = ((const uint16_t *)base)[i];
-        uint32_t u = ((uint32_t)h) << 16;
-        float f;
-        memcpy(&f, &u, sizeof f);
-        return (double)f;
-    }
-    return (double)((const float *)base)[i];
+    /* ORACLE_F16, IEEE binary16: 5 exponent bits with bias 15, 10 mantissa bits */
+    uint16_t b = ((const uint16_t *)base)[i];
+    int e = (b >> 10) & 0x1F, m = b & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);
+    else
+        v = ldexp(1024.0 + m, e - 25);
+    return (b & 0x8000) ? -v : v;
 }
 
 static int clamp_n(int32_t n, int max_blocks)
