@@ -253,6 +253,25 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- our arm
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu's, else /proc/cpuinfo's), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(case, target_s=10.0):
     import oracle
     oracle.build()
@@ -267,7 +286,8 @@ def cpu_baseline(case, target_s=10.0):
         per_q.append((time.perf_counter() - t0) / len(case.n_blocks[sl]))
         done += len(case.n_blocks[sl])
     us = statistics.mean(per_q) * case.nq * 1e6
-    return {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
+            "host_cores": os.cpu_count(),
             "sample": f"{done} of {case.nq} queries of the same workload (about {target_s:.0f} s), "
                       f"FP64 scores + full sort, single thread, scaled to the full call"}
 
