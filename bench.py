@@ -477,6 +477,22 @@ def run_ours(args):
     ad_out = torch.empty((adcase.nq, adcase.n_heads, 128), dtype=torch.float32, device=dev)
     ad_lse = torch.empty((adcase.nq, adcase.n_heads), dtype=torch.float32, device=dev)
 
+    # the prompt call: 256 queries at 131,072 tokens
+    pcase = inputs.prompt_case()
+    pq, pw, pkb, pnb = parity.to_device(pcase, dev)
+    pscores = torch.empty((pcase.nq, pcase.max_blocks), dtype=torch.float32, device=dev)
+    pids = torch.empty((pcase.nq, pcase.k), dtype=torch.int32, device=dev)
+    pws = qsa.alloc_workspace(pcase.nq, pcase.max_blocks, pcase.k, fused=True, device=dev)
+
+    def prompt_chained():
+        qsa.select(pq, pw, pkb, pnb, pcase.k, pids, pws, scores=pscores, active_blocks=pcase.active_blocks)
+
+    def prompt_fused():
+        qsa.select(pq, pw, pkb, pnb, pcase.k, pids, pws, fused=True, active_blocks=pcase.active_blocks)
+
+    def prompt_score():
+        qsa.block_scores(pq, pw, pkb, pnb, pscores, active_blocks=pcase.active_blocks, ws=pws)
+
     # the deep prompt with fp8 e4m3 queries and keys
     ecase = inputs.deep_e4m3_case()
     eq, ew, ekb, enb = parity.to_device(ecase, dev)
@@ -558,6 +574,8 @@ def run_ours(args):
     t_dec_f = timed_loop(torch, decode_fused, reps, flush, stream)
     t_dec_c = timed_loop(torch, decode_chained, reps, flush, stream)
     t_e2e = timed_loop(torch, e2e_step, args.steps, flush, stream, prime=False)
+    t_prompt = {name: timed_loop(torch, fn, reps, flush, stream)
+                for name, fn in (("chained", prompt_chained), ("fused", prompt_fused), ("scorer", prompt_score))}
     t_e4m3 = {name: timed_loop(torch, fn, reps, flush, stream)
               for name, fn in (("chained", e4m3_chained), ("fused", e4m3_fused), ("scorer", e4m3_score))}
     def deep_step():
@@ -643,6 +661,14 @@ def run_ours(args):
         "deep_parts_sum": us_main_median + attn["us_per_launch"],
         "decode": statistics.median(t_step["decode"]) * 1e3,
         "decode_parts_sum": statistics.median(t_dec_c) * 1e3 + attn["decode"]["us_per_call"]}
+    p_us = {k_: statistics.median(v_) * 1e3 for k_, v_ in t_prompt.items()}
+    p_n = int(pcase.n_blocks[0])
+    p_flops = 2.0 * pcase.nq * pcase.n_heads * 128 * p_n
+    p_tf = p_flops / (p_us["scorer"] * 1e-6) / 1e12
+    prompt = {"workload": pcase.name, "select_us": {"chained": p_us["chained"], "fused": p_us["fused"]},
+              "scorer": {"kernel": "scorer_tc_kernel<bf16, 16>", "us_per_launch": p_us["scorer"],
+                         "achieved": p_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": p_tf / peaks["bf16_tflops"], "per_launch": f"{p_flops:.4g} FLOP"}}
     e_us = {k_: statistics.median(v_) * 1e3 for k_, v_ in t_e4m3.items()}
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     e_tf = flops / (e_us["scorer"] * 1e-6) / 1e12
@@ -674,6 +700,7 @@ def run_ours(args):
                 "form": form},
         "selection_attention": attn,
         "e4m3_keys": e4m3,
+        "prompt_256q_131K": prompt,
         "topk_paths_us_cold": topk_paths,
         "warm_back_to_back_us_per_call": warm,
         "gpu_launches": args.steps * (1 if form == "fused" else 1 + topk_launches),
