@@ -202,10 +202,19 @@ def test_on_the_ids_of_the_select_path(qsa):
     check_rule_d(out[rows], lse[rows], ref, ref_lse, bounds)
 
 
+PATHS_B2B = ["auto", "split", "sample", "register", "radix", "warp"]
+
+
+@pytest.mark.parametrize("path", PATHS_B2B)
 @pytest.mark.parametrize("nq,fused", [(3, False), (3, True), (64, False), (64, True)])
-def test_select_then_attention_back_to_back(qsa, nq, fused):
+def test_select_then_attention_back_to_back(qsa, nq, fused, path):
     """The attention enqueued right behind the select that writes its ids (no host step
-    between, so it launches as the top-k's programmatic dependent)."""
+    between, so it launches as the programmatic dependent of whichever top-k kernel
+    wrote them)."""
+    if fused and path != "auto":
+        pytest.skip("the fused form takes the auto path only")
+    path_code = {"auto": qsa.PATH_AUTO, "split": qsa.PATH_SPLIT, "sample": qsa.PATH_SAMPLE,
+                 "register": qsa.PATH_REGISTER, "radix": qsa.PATH_RADIX, "warp": qsa.PATH_WARP}[path]
     sc = inputs.make_case(118 + nq, nq, 16, 2048, inputs.BF16, 131_072, 32, active_blocks=-1 if nq == 3 else 2048)
     q, w, kb, nb = to_device(sc)
     c = inputs.make_attention_case(119 + nq, nq, 4, 131_072, sc.tokens, 32)
@@ -218,7 +227,13 @@ def test_select_then_attention_back_to_back(qsa, nq, fused):
     torch.cuda.synchronize()
     for _ in range(3):   # repeated: every call's attention follows its own select
         ids.fill_(-9)
-        qsa.select(q, w, kb, nb, 32, ids, ws, scores=scores, fused=fused, active_blocks=sc.active_blocks)
+        try:
+            qsa.select(q, w, kb, nb, 32, ids, ws, scores=scores, fused=fused, active_blocks=sc.active_blocks,
+                       path=path_code)
+        except qsa.QSAError as e:
+            if e.status == qsa.ERR_UNSUPPORTED:
+                pytest.skip(f"{path} does not take this shape")
+            raise
         qsa.select_attention(qa, kc, vt, ids, nt, out, lse, scale=c.scale, ws=ws)
     torch.cuda.synchronize()
     assert qsa.read_flags(ws) & qsa.ERROR_FLAGS == 0
