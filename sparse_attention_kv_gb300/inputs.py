@@ -287,7 +287,7 @@ def random_ids(seed: int, n_blocks, k: int, n_valid=None) -> np.ndarray:
     return out
 
 
-def normal_bf16(seed: int, shape, chunks: int = 16, dtype: int = BF16) -> np.ndarray:
+def normal_16bit(seed: int, shape, chunks: int = 16, dtype: int = BF16) -> np.ndarray:
     """N(0,1) draws rounded to bf16 (or fp16) bits, in ``chunks`` equal slices of the flat array,
     slice i from the i-th PCG64 stream spawned from ``seed`` (filled in parallel
     threads; the values do not depend on the thread count)."""
@@ -318,8 +318,8 @@ def make_attention_case(seed: int, nq: int, n_kv_heads: int, capacity_tokens: in
     H = n_kv_heads * group
     draws = rng.standard_normal((nq, H, HEAD_DIM), dtype=np.float32)
     qa = to_f16_bits(draws) if dtype == F16 else to_bf16_bits(draws)
-    kc = normal_bf16(seed + 2, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
-    vc = normal_bf16(seed + 3, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
+    kc = normal_16bit(seed + 2, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
+    vc = normal_16bit(seed + 3, (n_kv_heads, capacity_tokens, HEAD_DIM), dtype=dtype)
     toks = np.broadcast_to(np.asarray(tokens, dtype=np.int64), (nq,)).astype(np.int32)
     if ids is None:
         ids = random_ids(seed + 1, blocks_for_tokens(toks), k, n_valid)

@@ -57,3 +57,13 @@ def test_e4m3_rounding_matches_torch_and_breaks_ties_to_even():
     ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     np.testing.assert_array_equal(ours, ref)
     assert inputs.to_e4m3_bits(np.float32([1e6, -1e6])).tolist() == [0x7E, 0xFE]   # saturated
+
+
+def test_parallel_normal_draws_do_not_depend_on_the_thread_count(monkeypatch):
+    import os
+    a = inputs.normal_16bit(11, (3, 1000, 128))
+    monkeypatch.setattr(os, "cpu_count", lambda: 1)     # one worker fills every slice in turn
+    b = inputs.normal_16bit(11, (3, 1000, 128))
+    np.testing.assert_array_equal(a, b)
+    c = inputs.normal_16bit(11, (3, 1000, 128), dtype=inputs.F16)
+    assert np.isfinite(c.view(np.float16)).all() and not np.array_equal(c, a)
