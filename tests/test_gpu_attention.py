@@ -83,6 +83,8 @@ WAVE_CASES = [
     # and empty rows among them
     (131, 80, 4, 4096, "ragged", 32, "random"),
     (132, 40, 8, 2048, "ragged", 7, None),
+    # 80 units at k = 64: unsplit, one CTA per SM, all 512 TMEM columns for the logits
+    (133, 80, 1, 8192, "ragged", 64, None),
 ]
 
 
