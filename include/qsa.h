@@ -133,7 +133,8 @@ qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
  * in 8 bits ("--kv int8"); the tensor-core 8-bit format of this GPU is e4m3.
  * Errors: QSA_ERR_INVALID_ARG for NULL q/w/kblk/n_blocks/scores, nq < 1,
  * head_dim != 128, unsupported n_heads, max_blocks outside [1, QSA_MAX_BLOCKS],
- * scores_stride < max_blocks, misaligned q/kblk, bad dtype.
+ * scores_stride < max_blocks, misaligned q/kblk, a dtype other than QSA_F32,
+ * QSA_BF16 or QSA_E4M3.
  */
 qsa_status qsa_block_scores(const void *q, const float *w, const void *kblk, qsa_dtype dt,
                             const int32_t *n_blocks, int nq, int n_heads, int head_dim,
