@@ -260,6 +260,26 @@ qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *
                                 float *lse, void *ws, size_t ws_bytes, qsa_stream stream);
 
 /*
+ * The V cache layout qsa_select_attention reads, from the token-row layout: for
+ * every KV head g and every block b in [first_block, first_block + n_blocks),
+ * vcache_t[g][b][d][r] = v[g][64 b + r][d] (d < 128, r < 64), copied bit for bit.
+ * A cache writer converts the blocks an append touched (the last, partial block
+ * again as it fills).  No passage of the source pages defines this call: it
+ * serves the layout reading of the attention (each block of V dimension-major, so
+ * the P.V product's operand is K-major).
+ *
+ *   v           [n_kv_heads][capacity][128] 16-bit values (bf16 or fp16), 16-byte aligned
+ *   vcache_t    [n_kv_heads][capacity / 64][128][64], same element size, 16-byte aligned;
+ *               must not overlap v
+ *   capacity    tokens per KV head, a positive multiple of 64
+ * Errors: QSA_ERR_INVALID_ARG for NULL or misaligned pointers, n_kv_heads < 1,
+ * capacity not a positive multiple of 64, n_kv_heads * capacity >= 2^30, a block
+ * range outside [0, capacity / 64), n_blocks < 0.
+ */
+qsa_status qsa_vcache_transpose(const void *v, void *vcache_t, int n_kv_heads, int capacity, int first_block,
+                                int n_blocks, qsa_stream stream);
+
+/*
  * Copy the workspace flags word (QSA_FLAG_* bits) to host `*flags`, waiting for
  * `stream` to finish; clear it on the device when `clear` is nonzero.
  */

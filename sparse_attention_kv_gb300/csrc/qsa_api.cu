@@ -331,6 +331,26 @@ qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *
     return launch_select_attention(a, static_cast<cudaStream_t>(stream));
 }
 
+qsa_status qsa_vcache_transpose(const void *v, void *vcache_t, int n_kv_heads, int capacity, int first_block,
+                                int n_blocks, qsa_stream stream) {
+    if (!v || !vcache_t) return fail(QSA_ERR_INVALID_ARG, "NULL v or vcache_t");
+    if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(vcache_t)) & 15u)
+        return fail(QSA_ERR_INVALID_ARG, "v and vcache_t must be 16-byte aligned");
+    if (n_kv_heads < 1) return fail(QSA_ERR_INVALID_ARG, "n_kv_heads must be >= 1 (got %d)", n_kv_heads);
+    if (capacity < 64 || capacity % 64)
+        return fail(QSA_ERR_INVALID_ARG, "capacity must be a positive multiple of 64 (got %d)", capacity);
+    if ((long long)n_kv_heads * capacity >= (1ll << 30))
+        return fail(QSA_ERR_INVALID_ARG, "n_kv_heads * capacity too large");
+    if (n_blocks < 0 || first_block < 0 || (long long)first_block + n_blocks > capacity / 64)
+        return fail(QSA_ERR_INVALID_ARG, "blocks [%d, %d + %d) outside [0, %d)", first_block, first_block, n_blocks,
+                    capacity / 64);
+    const size_t bytes = (size_t)n_kv_heads * capacity * QSA_HEAD_DIM * 2;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(v), b0 = reinterpret_cast<uintptr_t>(vcache_t);
+    if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(QSA_ERR_INVALID_ARG, "v and vcache_t overlap");
+    return launch_vcache_transpose(v, vcache_t, n_kv_heads, capacity, first_block, n_blocks,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 qsa_status qsa_read_flags(void *ws, uint32_t *flags, int clear, qsa_stream stream) {
     if (!ws || !flags) return fail(QSA_ERR_INVALID_ARG, "NULL workspace or flags");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -121,5 +121,7 @@ struct AttnArgs {
     uint32_t *flags;
 };
 qsa_status launch_select_attention(const AttnArgs &a, cudaStream_t s);
+qsa_status launch_vcache_transpose(const void *v, void *vcache_t, int n_kv_heads, int capacity, int first_block,
+                                   int n_blocks, cudaStream_t s);
 
 }  // namespace qsa

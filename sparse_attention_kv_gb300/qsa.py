@@ -34,7 +34,7 @@ ATTN_GROUP = 16
 ATTN_MAX_K = 64
 
 EXPORTS = ("qsa_workspace_bytes", "qsa_workspace_init", "qsa_block_scores", "qsa_block_topk",
-           "qsa_block_topk_static", "qsa_select", "qsa_select_attention", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
+           "qsa_block_topk_static", "qsa_select", "qsa_select_attention", "qsa_vcache_transpose", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
            "qsa_version")
 
 
@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     lib.qsa_select_attention.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                          ctypes.c_float, vp, vp, vp, sz, vp]
     lib.qsa_select_attention.restype = i32
+    lib.qsa_vcache_transpose.argtypes = [vp, vp, i32, i32, i32, i32, vp]
+    lib.qsa_vcache_transpose.restype = i32
     lib.qsa_read_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), i32, vp]
     lib.qsa_read_flags.restype = i32
     lib.qsa_auto_path.argtypes = [i32, i32, i32, i32]
@@ -252,6 +254,26 @@ def select_attention(qa: torch.Tensor, kcache: torch.Tensor, vcache_t: torch.Ten
                                   0 if ws is None else ws.numel(), _stream(stream))
     _check("qsa_select_attention", st)
     return out
+
+
+def vcache_transpose(v: torch.Tensor, vcache_t: torch.Tensor, first_block: int = 0, n_blocks: int | None = None,
+                     stream=None) -> torch.Tensor:
+    """vcache_t [Hkv, C/64, 128, 64] from v [Hkv, C, 128] (bf16 or fp16) for blocks
+    [first_block, first_block + n_blocks) (all by default)."""
+    lib = load()
+    _contig(v, "v")
+    _contig(vcache_t, "vcache_t")
+    if v.dtype not in (torch.bfloat16, torch.float16) or vcache_t.dtype != v.dtype:
+        raise ValueError("v and vcache_t must both be bfloat16 or both float16")
+    Hkv, C, D = v.shape
+    if D != 128 or tuple(vcache_t.shape) != (Hkv, C // 64, 128, 64):
+        raise ValueError("v must be [Hkv, C, 128] and vcache_t [Hkv, C/64, 128, 64]")
+    if n_blocks is None:
+        n_blocks = C // 64 - first_block
+    st = lib.qsa_vcache_transpose(_dptr(v, "v"), _dptr(vcache_t, "vcache_t"), Hkv, C, first_block, n_blocks,
+                                  _stream(stream))
+    _check("qsa_vcache_transpose", st)
+    return vcache_t
 
 
 def read_flags(ws: torch.Tensor, clear: bool = True, stream=None) -> int:

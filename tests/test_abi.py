@@ -131,6 +131,18 @@ def test_select_attention_rejects_bad_arguments_before_launch(lib, case, status)
     assert lib.qsa_last_error().decode()
 
 
+@pytest.mark.parametrize("case", [
+    dict(v=None), dict(v=FAKE + 2), dict(n_kv=0), dict(capacity=100), dict(capacity=0),
+    dict(first=-1), dict(n=-1), dict(first=60, n=5), dict(vt=FAKE + 4096),   # the last: overlapping buffers
+])
+def test_vcache_transpose_rejects_bad_arguments(lib, case):
+    a = dict(v=FAKE, vt=FAKE + (1 << 24), n_kv=2, capacity=4096, first=0, n=64)
+    a.update(case)
+    st = lib.qsa_vcache_transpose(a["v"], a["vt"], a["n_kv"], a["capacity"], a["first"], a["n"], None)
+    assert st == qsa.ERR_INVALID_ARG
+    assert lib.qsa_last_error().decode()
+
+
 def test_topk_rejects_bad_arguments_before_launch(lib):
     st = lib.qsa_block_topk(FAKE, 100, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 0, None)
     assert st == qsa.ERR_INVALID_ARG   # stride < max_blocks

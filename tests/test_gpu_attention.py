@@ -245,6 +245,23 @@ def test_select_then_attention_back_to_back(qsa, nq, fused, path):
     check_rule_d(out.cpu().numpy()[rows], lse.cpu().numpy()[rows], ref, ref_lse, bounds)
 
 
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F16], ids=["bf16", "fp16"])
+def test_vcache_transpose_is_the_block_transpose(qsa, dtype):
+    """The library's layout conversion, bit for bit, in full and over a block range."""
+    c = inputs.make_attention_case(140, 1, 3, 4096, 4096, 1, dtype=dtype)
+    tdt = torch.float16 if dtype == inputs.F16 else torch.bfloat16
+    v = torch.from_numpy(c.vc.view(np.int16)).view(tdt).cuda()
+    want = inputs.vcache_blocks_transposed(c.vc)
+    vt = torch.zeros((3, 64, 128, 64), dtype=tdt, device="cuda")
+    qsa.vcache_transpose(v, vt)
+    np.testing.assert_array_equal(vt.cpu().view(torch.int16).numpy().view(np.uint16), want)
+    vt.zero_()
+    qsa.vcache_transpose(v, vt, first_block=10, n_blocks=7)
+    got = vt.cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got[:, 10:17], want[:, 10:17])
+    assert (got[:, :10] == 0).all() and (got[:, 17:] == 0).all()
+
+
 @pytest.fixture(scope="module")
 def deep_attention():
     """The bench's configuration: 256 queries x 64 heads (4 GQA groups of 16),
