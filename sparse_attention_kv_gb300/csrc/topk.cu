@@ -4,10 +4,12 @@
 // launched as a programmatic dependent of the kernel before it on the stream and
 // waits at entry until that kernel has completed (in a chained select its CTAs
 // take SMs while the scorer drains).
-//  * warp:     k <= 32, rows of up to 8,192 blocks: one CTA per query, one warp
-//    per 1,024-block chunk bounds, filters and ranks its chunk in registers, and
-//    the chunks' lists are merged by exact ranks (warp_topk.cuh); the AUTO choice
-//    wherever it applies.
+//  * warp:     k <= 32, rows of up to 8,192 blocks: one CTA per query holds its
+//    row in registers (one warp per 1,024-block chunk), bounds the k-th largest
+//    score from below with maxima of the whole row, keeps the few scores at or
+//    above the bound and ranks them exactly; heavy ties take a per-chunk select
+//    and a merge of the chunks' lists (warp_topk.cuh).  The AUTO choice wherever
+//    it applies.
 //  * register: one CTA per query holds its whole row in registers (<= 8,192
 //    blocks: 256 threads x 32) and selects with no re-read -- the "register
 //    kernel" the pages name for contexts within its reach (Strata PR #3987,
@@ -28,6 +30,7 @@
 //    selected block is among its chunk's candidates (Strata PR #3987,
 //    "Approach").
 #include <algorithm>
+#include <cstddef>
 #include <cstdio>
 #include <mutex>
 
@@ -435,42 +438,76 @@ __global__ void __launch_bounds__(kNT, 2) topk_split_kernel(TopkArgs a, int chun
 // ---------------------------------------------------------------------------- warp path
 //
 // k <= 32, rows of up to NW * 1,024 blocks, one CTA of NW warps per query.  Warp
-// w takes blocks [1024 w, 1024 (w + 1)) of the row into registers (one read of
-// HBM), bounds the chunk's k-th largest key from below with the k-th largest of
-// the lanes' top-2 keys, keeps the entries at or above it (a few more than k on
-// continuous scores) and ranks them exactly: its chunk's top k, descending, in
-// shared memory.  The chunks' lists are then merged by exact ranks (one thread per
-// candidate, binary searches in the other lists).  A query's selection restricted
-// to a chunk is a prefix of that chunk's order, so every selected block is among
-// its chunk's k (the split of Strata PR #3987, section "Approach").  Heavy ties
-// (more than 64 entries at a chunk's bound) take the radix warp select for that
-// chunk instead.
+// w holds blocks [1024 w, 1024 (w + 1)) of the row in registers (one read of
+// HBM): lane l the entries 1024 w + 4 (l + 32 t) + c, t < 8, c < 4.
+//
+// Row bound.  Each lane takes the largest of its 32 scores.  Each warp whose
+// chunk fills all 32 lanes takes the r-th largest of its lane maxima, r =
+// ceil(k / such warps), and the row bound B is the smallest of those: every such
+// warp has r lanes whose maxima (distinct entries) reach B, so at least k
+// entries of the row score >= B and every selected block is among them.  On
+// continuous scores B sits a little below the row's k-th largest score (about
+// 50 entries reach it at 8,125 blocks and k = 32), so one compare per score
+// keeps the survivors.  They go to shared memory packed as (key, ~id) -- a
+// total order that is exactly the selection order -- and are ranked exactly
+// (a few threads per survivor); the k of rank below k are the selection,
+// emitted in ascending id order.  This is the one-read candidate filter of
+// "#2093 sm_75: the prompt path's top-k with one full read of the scores"
+// (steps 2-3) with the bound drawn from maxima of the whole row rather than a
+// 1-in-32 sample, so "at least k candidates" holds by construction.
+//
+// More survivors than the on-chip list holds (heavy ties) take the per-chunk
+// path below, which rows of at most one chunk take directly (their bound from
+// the lanes' top-2 keys is the tighter one there).
 
 constexpr int kWarpChunk = 1024;   // blocks per warp (CL); 512-block chunks measured slower even for 3 queries
+constexpr int kRowCap = 256;       // survivors of the row bound held on chip
 constexpr size_t kWarpTwoPerSmBytes = 90 * 1024;   // dynamic shared memory that leaves room for two CTAs per SM
 
-template <int NW, int CL>
-__global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
-    wait_prior_grid();   // the scores may come from the kernel launched just before
-    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
-    __shared__ __align__(16) uint32_t scratch[NW][256];   // per warp: candidates / histogram
-    __shared__ __align__(16) uint64_t lists[NW * 32];      // per chunk: its top k, descending
-    const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
-    const int k = a.k;
-    int32_t *out = a.ids + (size_t)q * k;
-    if (n <= k) {
-        emit_all(n, k, out);
-        return;
+// v[b] for a runtime b < N (N a power of two) without indexing registers: a tree of
+// selects on the bits of b.
+template <int N>
+__device__ __forceinline__ float pick(const float (&v)[N], int b) {
+    static_assert((N & (N - 1)) == 0 && N >= 2, "power of two");
+    float y[N / 2];
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) y[j] = (b & 1) ? v[2 * j + 1] : v[2 * j];
+    if constexpr (N == 2) {
+        return y[0];
+    } else {
+        return pick<N / 2>(y, b >> 1);
     }
-    const float *row = a.scores + (size_t)q * a.stride;
-    uint32_t *h = scratch[warp];
+}
+
+template <int NW>
+struct __align__(16) WarpPathSmem {
+    uint32_t scratch[NW][256];   // per-chunk path: per warp candidates / histogram
+    uint64_t lists[NW * 32];     // per-chunk path: each chunk's top k, descending
+    uint64_t cand[kRowCap];      // row-bound survivors, packed
+    __align__(16) int32_t sel[32];   // selected ids by rank (read as int4)
+    uint32_t wbound[8];          // each full warp's r-th largest lane-maximum key
+    int cnt;                     // survivors
+};
+
+// The per-chunk path.  Warp w bounds its chunk's k-th largest key from below with
+// the k-th largest of the lanes' top-2 keys, keeps the entries at or above it (a
+// few more than k on continuous scores) and ranks them exactly: its chunk's top
+// k, descending, in shared memory.  The chunks' lists are then merged by exact
+// ranks (one thread per candidate, binary searches in the other lists).  A
+// query's selection restricted to a chunk is a prefix of that chunk's order, so
+// every selected block is among its chunk's k (the split of Strata PR #3987,
+// section "Approach").  Heavy ties (more than 64 entries at a chunk's bound)
+// take the radix warp select for that chunk.  Every thread of the CTA calls it.
+template <int NW, int CL>
+__device__ __noinline__ void warp_chunk_select(const float *row, int n, int k, int32_t *out, WarpPathSmem<NW> &sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t *h = sm.scratch[warp];
     uint64_t *buf = reinterpret_cast<uint64_t *>(h);
     for (int i = lane; i < 256; i += 32) h[i] = 0u;
     __syncwarp();
     const int lo = warp * CL;
     const int len = min(CL, n - lo);
-    uint64_t *dst = lists + warp * k;
+    uint64_t *dst = sm.lists + warp * k;
     if (len > k) {
         const float *r = row + lo;
         const float4 *r4 = reinterpret_cast<const float4 *>(r);
@@ -500,7 +537,7 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
             if (lane < k) dst[lane] = ~v;
         }
     } else if (len > 0) {
-        uint64_t v = lane < len ? ~pack_cand(score_key(__ldcs(row + lo + lane)), lo + lane) : ~0ull;
+        uint64_t v = lane < len ? ~pack_cand(score_key(__ldg(row + lo + lane)), lo + lane) : ~0ull;
         warp_sort32_asc(v);
         if (lane < len) dst[lane] = ~v;
     }
@@ -509,32 +546,230 @@ __global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
     // is its index in its own list plus, for every other list, the number of entries
     // above it (a binary search); packed values are distinct, so the ranks are a
     // permutation and exactly k candidates rank below k.  One thread per candidate.
-    __shared__ int32_t sel[32];
     const int nch = (n + CL - 1) / CL;
     auto cnt_of = [&](int c) { return c < nch ? min(k, n - c * CL) : 0; };
     if (lane < cnt_of(warp)) {
-        const uint64_t x = lists[warp * k + lane];
+        const uint64_t x = sm.lists[warp * k + lane];
         int rank = lane;
 #pragma unroll
         for (int b = 0; b < NW; ++b) {
             if (b == warp) continue;
             const int cb = cnt_of(b);
-            const uint64_t *lb = lists + b * k;
+            const uint64_t *lb = sm.lists + b * k;
             int pos = 0;   // entries of list b above x
 #pragma unroll
             for (int step = 32; step >= 1; step >>= 1)
                 if (pos + step <= cb && lb[pos + step - 1] > x) pos += step;
             rank += pos;
         }
-        if (rank < k) sel[rank] = cand_id(x);
+        if (rank < k) sm.sel[rank] = cand_id(x);
     }
     __syncthreads();
     if (warp != 0) return;
     if (lane < k) {   // ascending ids: each id's slot is the number of selected ids below it
-        const int32_t id = sel[lane];
+        const int32_t id = sm.sel[lane];
         int below = 0;
-        for (int t = 0; t < k; ++t) below += sel[t] < id;
+        for (int t = 0; t < k; ++t) below += sm.sel[t] < id;
         out[below] = id;
+    }
+}
+
+// Exact ranks of m distinct packed candidates cand[0..m) (rank 0 = the largest):
+// sel[r] = the id of the candidate of rank r, for r < k (exactly k rank below k when
+// m >= k).  A rank is the number of candidates above; P threads per candidate (a
+// power of two dividing the warp) share the count.  Every thread of the NT-thread
+// block calls it.
+template <int NT>
+__device__ __forceinline__ void rank_survivors(const uint64_t *cand, int m, int k, int32_t *sel) {
+    if (m <= 64) {   // the common case: every compare unrolled, P fixed
+        constexpr int P = NT / 64;
+        const int i = (int)threadIdx.x / P, sub = (int)threadIdx.x % P;
+        const uint64_t c = i < m ? cand[i] : 0ull;
+        int rk = 0;
+#pragma unroll
+        for (int t = 0; t < 64 / P; ++t) {
+            const int j = sub + P * t;
+            rk += j < m && cand[j] > c;
+        }
+#pragma unroll
+        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
+        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
+        return;
+    }
+    int lp = 0;   // P = 1 << lp <= 8, as many as the block holds
+    while (lp < 3 && (2 * m << lp) <= NT) ++lp;
+    const int P = 1 << lp;
+    for (int b0 = 0; b0 < m * P; b0 += NT) {
+        const int e = b0 + (int)threadIdx.x;
+        const int i = e >> lp, sub = e & (P - 1);
+        const uint64_t c = i < m ? cand[i] : 0ull;
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int j = sub;
+        for (; j + 3 * P < m; j += 4 * P) {
+            r0 += cand[j] > c;
+            r1 += cand[j + P] > c;
+            r2 += cand[j + 2 * P] > c;
+            r3 += cand[j + 3 * P] > c;
+        }
+        for (; j < m; j += P) r0 += cand[j] > c;
+        int rk = (r0 + r1) + (r2 + r3);
+        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
+        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
+    }
+}
+
+template <int NW, int CL>
+__global__ void __launch_bounds__(NW * 32, 2) topk_warp_kernel(TopkArgs a) {
+    wait_prior_grid();   // the scores may come from the kernel launched just before
+    allow_dependent_launch();   // a consumer of the ids (the attention) may launch and wait
+    static_assert(NW <= 8 && offsetof(WarpPathSmem<NW>, sel) % 16 == 0, "sel is read as int4");
+    __shared__ WarpPathSmem<NW> sm;
+    const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = a.k;
+    int32_t *out = a.ids + (size_t)q * k;
+    const float *row = a.scores + (size_t)q * a.stride;
+    if constexpr (NW == 1) {
+        const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
+        if (n <= k) {
+            emit_all(n, k, out);
+            return;
+        }
+        warp_chunk_select<NW, CL>(row, n, k, out, sm);
+    } else {
+        constexpr int NV = CL / 128;   // float4 loads per lane
+        constexpr int NT = NW * 32;
+        const float kNegInf = __int_as_float(0xff800000);
+        // 1. this warp's chunk into registers.  Every entry below the host-visible bound
+        //    lies in the caller's row (stride >= bound), so the loads go out together
+        //    with the load of n_blocks[q] instead of after it; entries at or past n are
+        //    then set to -inf.
+        const int lo = warp * CL;
+        const int cap = max(0, min(CL, a.bound - lo));
+        const float *r = row + lo;
+        const float4 *r4 = reinterpret_cast<const float4 *>(r);
+        const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
+        float x[4 * NV];
+        if (vec && cap == CL) {
+#pragma unroll
+            for (int t = 0; t < NV; ++t) {
+                const float4 f = __ldg(r4 + lane + 32 * t);
+                x[4 * t + 0] = f.x;
+                x[4 * t + 1] = f.y;
+                x[4 * t + 2] = f.z;
+                x[4 * t + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < NV; ++t) {
+                const int v = lane + 32 * t;
+                if (vec && 4 * v + 3 < cap) {
+                    const float4 f = __ldg(r4 + v);
+                    x[4 * t + 0] = f.x;
+                    x[4 * t + 1] = f.y;
+                    x[4 * t + 2] = f.z;
+                    x[4 * t + 3] = f.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) x[4 * t + c] = 4 * v + c < cap ? __ldg(r + 4 * v + c) : kNegInf;
+                }
+            }
+        }
+        const int n = clamp_blocks(a.n_blocks, q, a.bound, a.flags);
+        if (n <= k) {
+            emit_all(n, k, out);
+            return;
+        }
+        const int len = max(0, min(CL, n - lo));
+        if (len < cap) {
+#pragma unroll
+            for (int t = 0; t < NV; ++t)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (4 * (lane + 32 * t) + c >= len) x[4 * t + c] = kNegInf;
+        }
+        float m4[NV];
+#pragma unroll
+        for (int t = 0; t < NV; ++t) m4[t] = fmaxf(fmaxf(x[4 * t], x[4 * t + 1]), fmaxf(x[4 * t + 2], x[4 * t + 3]));
+#pragma unroll
+        for (int s = 1; s < NV; s <<= 1)
+#pragma unroll
+            for (int t = 0; t + s < NV; t += 2 * s) m4[t] = fmaxf(m4[t], m4[t + s]);
+        const float mx = m4[0];
+        // 2. the row bound: warps whose chunk holds >= 128 entries have an entry on every
+        //    lane; each takes the r-th largest of its lanes' maxima
+        const int nfull = n >= 128 ? min(NW, (n - 128) / CL + 1) : 0;
+        if (warp < nfull) {
+            const int r_th = (k + nfull - 1) / nfull;
+            uint32_t kk = score_key(mx), res = 0u;
+            for (int it = 0; it < r_th; ++it) {
+                res = __reduce_max_sync(kFull, kk);
+                const unsigned win = __ballot_sync(kFull, kk == res);
+                if (lane == __ffs(win) - 1) kk = 0u;   // 0 is below every score's key
+            }
+            if (lane == 0) sm.wbound[warp] = res;
+        }
+        if (threadIdx.x == 0) sm.cnt = 0;
+        __syncthreads();
+        uint32_t wb[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) wb[w] = w < nfull ? sm.wbound[w] : 0xffffffffu;
+#pragma unroll
+        for (int s = 1; s < NW; s <<= 1)
+#pragma unroll
+            for (int w = 0; w + s < NW; w += 2 * s) wb[w] = min(wb[w], wb[w + s]);
+        const uint32_t B = wb[0];
+        // with no full warp (n < 128) every entry is a survivor; a bound of -inf (scores
+        // of -inf) would also pass the padding, so then entries are tested against len
+        const float Bf = nfull > 0 ? key_float(B) : kNegInf;
+        const bool guard = !(Bf > kNegInf);
+        // 3. survivors, the scores >= B: a bit per entry of the lane (no branches), a
+        //    shared atomic for each lane that has any, then each such lane writes its few
+        //    survivors, each value picked from the lane's registers by the bits of its
+        //    position
+        uint32_t sv[4] = {0u, 0u, 0u, 0u};   // four partial masks: short dependency chains
+#pragma unroll
+        for (int t = 0; t < NV; ++t)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (x[4 * t + c] >= Bf) sv[c] |= 1u << (4 * t + c);
+        uint32_t surv = (sv[0] | sv[1]) | (sv[2] | sv[3]);
+        if (guard) {
+#pragma unroll
+            for (int t = 0; t < NV; ++t)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (4 * (lane + 32 * t) + c >= len) surv &= ~(1u << (4 * t + c));
+        }
+        int pos = surv ? atomicAdd(&sm.cnt, __popc(surv)) : 0;
+        while (surv) {
+            const int bit = __ffs(surv) - 1;
+            surv &= surv - 1u;
+            const int i = 4 * (lane + 32 * (bit >> 2)) + (bit & 3);
+            if (pos < kRowCap) sm.cand[pos] = pack_cand(score_key(pick<4 * NV>(x, bit)), lo + i);
+            ++pos;
+        }
+        __syncthreads();
+        const int m = sm.cnt;
+        if (m >= k && m <= kRowCap) {
+            // 4. exact ranks of the survivors; the k of rank below k are the selection
+            rank_survivors<NT>(sm.cand, m, k, sm.sel);
+            __syncthreads();
+            if (warp == 0 && lane < k) {   // 5. the k ids, ascending: an id's slot is the number below it
+                const int32_t id = sm.sel[lane];
+                int below = 0;
+                const int4 *s4 = reinterpret_cast<const int4 *>(sm.sel);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int4 v = s4[t];
+                    below += (4 * t + 0 < k && v.x < id) + (4 * t + 1 < k && v.y < id) +
+                             (4 * t + 2 < k && v.z < id) + (4 * t + 3 < k && v.w < id);
+                }
+                out[below] = id;
+            }
+            return;
+        }
+        // heavy ties: more survivors than the list holds
+        warp_chunk_select<NW, CL>(row, n, k, out, sm);
     }
 }
 
