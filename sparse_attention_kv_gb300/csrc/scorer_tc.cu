@@ -92,7 +92,6 @@ struct Ctrl {
     uint64_t tfull[2], tempty[2];
     uint32_t tmem_base;
     int abort;
-    int maxn;
     int last;
     __align__(16) float w[256];
     int nb[256];
@@ -355,6 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_begin = blockIdx.x * p.tiles_per_cta;
     const int t_cap = min(p.tiles_per_cta, p.tiles_total - t_begin);  // tiles under the bound
 
+    // TMEM first (warp 1), while the barriers are set up: nothing the MMA warp needs
+    // waits for the reads of w and n_blocks, which only the epilogue uses
+    if (warp == 1 && t_cap > 0) {
+        tmem_alloc(&ct.tmem_base, (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
     if (tid == 32) {
         for (int s = 0; s < 4; ++s) {
             mbar_init(&ct.full[s], 1);
@@ -375,15 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
     }
+    tc_fence_before();
     __syncthreads();
-    // The query tile and the first stages are requested before the group's block
-    // counts are known, so their latency overlaps the reads of w and n_blocks.
+    tc_fence_after();
+    // The query tile and the first stages are requested at once.  The tiles run to the
+    // host-visible bound: the TMA and MMA warps never wait for n_blocks, and the
+    // epilogue stores only the rows below each query's count.
+    const int ntiles = t_cap;
     int issued = 0;
-    if (tid == 0) {
+    if (tid == 0 && ntiles > 0) {
         mbar_expect_tx(&ct.bfull, (uint32_t)(C::kAtoms * bn * 128));
         for (int a = 0; a < C::kAtoms; ++a)
             tma_load_2d(sB + a * bn * 128, &tm_q, &ct.bfull, a * C::kEPA, q0 * H);
-        const int pre = min(L::kStages, t_cap);
+        const int pre = min(L::kStages, ntiles);
         for (int i = 0; i < pre; ++i) {
             mbar_expect_tx(&ct.full[i], (uint32_t)(C::kAtoms * kAtomA));
             for (int a = 0; a < C::kAtoms; ++a)
@@ -391,38 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued = pre;
     }
-    for (int i = tid; i < qv * H; i += kThreads) ct.w[i] = p.w[(size_t)q0 * H + i];
-    if (warp == 0) {
-        int mx = 0;
-        for (int j = lane; j < qv; j += 32) {
+    if (ntiles <= 0) {
+        // no tile under the bound (fused form, empty contexts): the block counts for its
+        // selection step
+        for (int j = tid; j < qv; j += kThreads) {
             int n = p.n_blocks[q0 + j];
             if (n < 0 || n > p.bound) {
                 if (p.flags && blockIdx.x == 0) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
                 n = n < 0 ? 0 : p.bound;
             }
             ct.nb[j] = n;
-            mx = max(mx, n);
         }
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (lane == 0) ct.maxn = mx;
-    }
-    __syncthreads();
-    const int ntiles_g = (ct.maxn + kBM - 1) / kBM;
-    const int ntiles = min(t_begin + p.tiles_per_cta, ntiles_g) - t_begin;
-    if (ntiles <= 0) {
-        if (tid == 0) {   // nothing to compute: let the early loads land
-            for (int j = 0; j < issued; ++j) mbar_drain(&ct.full[j], 0);
-            mbar_drain(&ct.bfull, 0);
-        }
-        if constexpr (!FUSED) return;
+        __syncthreads();
     } else {
-    if (warp == 1) {
-        tmem_alloc(&ct.tmem_base, (uint32_t)p.tmem_cols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = ct.tmem_base;
     const int buf_cols = p.tmem_cols / 2;
 
@@ -448,6 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- MMA issuer
             const uint32_t id = idesc(C::kFmt, kBM, bn);
+            // Every descriptor is its stage's or the query tile's base plus a constant
+            // (start addresses in 16-byte units, all below 2^14): this warp shares its
+            // scheduler with busy epilogue warps, so each MMA costs it a few integer adds.
+            uint64_t db[C::kAtoms * 4], dbl[F32 ? C::kAtoms * 4 : 1];
+#pragma unroll
+            for (int a = 0; a < C::kAtoms; ++a)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    db[a * 4 + kk] = sdesc(smem_u32(sB) + (uint32_t)(a * bn * 128 + kk * 32));
+                    if constexpr (F32) dbl[a * 4 + kk] = sdesc(smem_u32(sBlo) + (uint32_t)(a * bn * 128 + kk * 32));
+                }
             bool ok = mbar_wait(F32 ? &ct.bsplit : &ct.bfull, 0, abort_flag);
             tc_fence_after();
             for (int i = 0; ok && i < ntiles; ++i) {
@@ -459,21 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(F32 ? &ct.split[s] : &ct.full[s], ph, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * buf_cols);
-                const uint32_t a0 = smem_u32(sA + s * L::kAStage);
-                const uint32_t al0 = smem_u32(sAlo + s * L::kAStage);
-                const uint32_t b0 = smem_u32(sB);
-                const uint32_t bl0 = smem_u32(sBlo);
+                const uint64_t da = sdesc(smem_u32(sA + s * L::kAStage));
+                const uint64_t dal = F32 ? sdesc(smem_u32(sAlo + s * L::kAStage)) : 0ull;
 #pragma unroll
                 for (int a = 0; a < C::kAtoms; ++a) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t aoff = (uint32_t)(a * kAtomA + kk * 32);
-                        const uint32_t boff = (uint32_t)(a * bn * 128 + kk * 32);
+                        const uint64_t aoff = (uint64_t)((a * kAtomA + kk * 32) >> 4);
                         const uint32_t acc = (a | kk) != 0 ? 1u : 0u;
-                        mma<C::kKind>(d, sdesc(a0 + aoff), sdesc(b0 + boff), id, acc);
+                        mma<C::kKind>(d, da + aoff, db[a * 4 + kk], id, acc);
                         if constexpr (F32) {
-                            mma<C::kKind>(d, sdesc(a0 + aoff), sdesc(bl0 + boff), id, 1u);
-                            mma<C::kKind>(d, sdesc(al0 + aoff), sdesc(b0 + boff), id, 1u);
+                            mma<C::kKind>(d, da + aoff, dbl[a * 4 + kk], id, 1u);
+                            mma<C::kKind>(d, dal + aoff, db[a * 4 + kk], id, 1u);
                         }
                     }
                 }
@@ -489,6 +487,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The kEpiParts warps of a TMEM lane quarter (warp % 4) split the tile's
         // 16-column chunks (16/H queries each) between them.
         const int et = tid - 64;                 // 0..511
+        // the group's weights and block counts (clamped), for the epilogue warps only
+        for (int i = et; i < qv * H; i += kEpi) ct.w[i] = p.w[(size_t)q0 * H + i];
+        for (int j = et; j < qv; j += kEpi) {
+            int n = p.n_blocks[q0 + j];
+            if (n < 0 || n > p.bound) {
+                if (p.flags && blockIdx.x == 0) atomicOr(p.flags, QSA_FLAG_NBLOCKS_CLAMPED);
+                n = n < 0 ? 0 : p.bound;
+            }
+            ct.nb[j] = n;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory");
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
         const int part = (warp - 2) >> 2;        // 0..kEpiParts-1
         const int row = quarter * 32 + lane;
@@ -538,6 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < kMaxChunks; ++cc)
                 if (cc < nc) reg_fence(v[cc]);
+            // the accumulators are in registers: the buffer goes back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ct.tempty[b]);
 #pragma unroll
             for (int cc = 0; cc < kMaxChunks; ++cc) {
                 if (cc < nc) {
@@ -553,9 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ct.tempty[b]);
         }
     }
     __syncthreads();
