@@ -21,9 +21,10 @@
  *
  * Conventions for every entry point:
  *  - Every pointer argument except the ones marked "host" is DEVICE memory owned
- *    by the caller.  The library never allocates or frees memory on a call, never
- *    synchronises the device, and keeps no global mutable device state: all
- *    scratch lives in the caller's workspace.
+ *    by the caller.  The library never allocates or frees memory on a call and
+ *    never synchronises the device.  Scratch lives in the caller's workspace, with
+ *    one exception: qsa_block_topk_static uses a fixed scratch array compiled into
+ *    the library (see there); no other entry point keeps device state between calls.
  *  - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
  *    and runs asynchronously; the return value reports host-side validation and
  *    launch errors only.  Device-side contract violations are recorded as bits in
@@ -76,8 +77,10 @@ typedef enum {
     QSA_PATH_SAMPLE = 2,   /* one read against a sampled lower bound (+ radix fallback) */
     QSA_PATH_REGISTER = 3, /* whole row in registers, one CTA per query */
     QSA_PATH_RADIX = 4,    /* multi-pass radix select over global memory, any size */
-    QSA_PATH_WARP = 5      /* k <= 32: one warp per 1,024-block chunk bounds, filters and ranks its
-                              chunk in registers, one warp merges (rows of up to 8,192 blocks) */
+    QSA_PATH_WARP = 5      /* k <= 32, rows of up to 8,192 blocks held in registers (one warp per
+                              1,024): a bound from the row's lane maxima keeps a few more than k
+                              scores, which are ranked exactly; heavy ties take a per-chunk select
+                              and merge */
 } qsa_path;
 
 typedef void *qsa_stream; /* a cudaStream_t */
@@ -144,7 +147,9 @@ qsa_status qsa_block_scores(const void *q, const float *w, const void *kblk, qsa
 /*
  * Block top-k over given fp32 scores.
  *
- *   scores   [nq][scores_stride] fp32 (NaN is outside the contract; -0 == +0)
+ *   scores   [nq][scores_stride] fp32 (NaN is outside the contract; -0 == +0); every
+ *            entry below the bound (active_blocks, else max_blocks) must be readable
+ *            memory: entries at or past n_blocks[q] may be read but never affect ids
  *   n_blocks [nq] int32 on the DEVICE, clamped as for qsa_block_scores
  *   k        1 <= k <= QSA_MAX_K
  *   ids      [nq][k] int32 out: the selected block ids in ascending order; when
@@ -174,8 +179,10 @@ qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int3
  * QSA_ERR_WORKSPACE and nothing is launched.  The call never allocates.
  *
  * The first call on each device looks up the scratch's device address (a CUDA
- * runtime query, with that device current) and caches it; make that first call
- * before any stream capture.  All calls share the one scratch array: the parts
+ * runtime query, with that device current) and caches it, and looks it up again
+ * when the device's context has been replaced (after cudaDeviceReset); make that
+ * first call before any stream capture.  A call rejected by its argument checks
+ * enqueues nothing, not even the clear below.  All calls share the one scratch array: the parts
  * that must start at zero are cleared on `stream` at the start of every call,
  * and calls that can overlap on the GPU (different streams or host threads)
  * race with each other.  The device flags of these calls are not readable.
@@ -183,6 +190,53 @@ qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int3
 qsa_status qsa_block_topk_static(const float *scores, int64_t scores_stride, const int32_t *n_blocks, int nq,
                                  int max_blocks, int active_blocks, int k, int32_t *ids, qsa_path path,
                                  qsa_stream stream);
+
+/*
+ * KV-sharded selection, stage A: the candidates of one shard of the KV blocks.
+ * A query's selection restricted to a subset of its blocks is a prefix of that
+ * subset's selection order (score descending, block id ascending), so the k best
+ * blocks of every shard, merged by qsa_merge_candidates, select exactly the blocks
+ * one call over all of them selects (Strata PR #3987, section "Approach": each
+ * chunk keeps its top k, one CTA per query selects over the union).  The shards
+ * may live on different GPUs: each computes its candidates, an all-gather collects
+ * nq x k of them per shard, and every GPU merges.
+ *
+ *   scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, ws, ws_bytes,
+ *   path           as for qsa_block_topk, over this shard's blocks (local ids 0 ..
+ *                  n_blocks[q] - 1)
+ *   block_offset   host int: the global id of the shard's first block; ids
+ *                  block_offset + max_blocks - 1 must stay below 2^31 - 1
+ *   cand_ids       [nq][k] int32 out: the shard's selection as global ids
+ *                  (block_offset + local id), ascending, -1 padded when n_blocks[q] < k
+ *   cand_scores    [nq][k] fp32 out: each candidate's score (-inf where the id is -1)
+ *
+ * Two launches on `stream`: the top-k (any path) into cand_ids, then a kernel that
+ * reads the candidates' scores and offsets their ids.
+ * Errors: as qsa_block_topk, plus QSA_ERR_INVALID_ARG for NULL cand_scores /
+ * cand_ids or a block_offset outside the range above.
+ */
+qsa_status qsa_block_candidates(const float *scores, int64_t scores_stride, const int32_t *n_blocks, int nq,
+                                int max_blocks, int active_blocks, int k, int32_t block_offset, float *cand_scores,
+                                int32_t *cand_ids, void *ws, size_t ws_bytes, qsa_path path, qsa_stream stream);
+
+/*
+ * KV-sharded selection, stage B: the k blocks of highest score over every shard's
+ * candidates, ties to the lower global id, emitted as ids in ascending order (-1
+ * padded when all shards together hold fewer than k candidates).
+ *
+ *   cand_scores  [n_shards][nq][k] fp32: the shards' qsa_block_candidates outputs,
+ *                shard-major (the layout an all-gather of the [nq][k] arrays leaves)
+ *   cand_ids     [n_shards][nq][k] int32: their global ids; entries < 0 are empty;
+ *                the shards' ids must be distinct (disjoint block ranges)
+ *   ids          [nq][k] int32 out
+ *
+ * One launch (one CTA per query), no workspace.
+ * Errors: QSA_ERR_INVALID_ARG for NULL pointers, nq < 1, k outside [1, QSA_MAX_K],
+ * n_shards < 1, n_shards x nq x k >= 2^31; QSA_ERR_UNSUPPORTED when n_shards x k
+ * exceeds 4,096 candidates per query.
+ */
+qsa_status qsa_merge_candidates(const float *cand_scores, const int32_t *cand_ids, int n_shards, int nq, int k,
+                                int32_t *ids, qsa_stream stream);
 
 /*
  * Score then select, in one call.
@@ -272,8 +326,8 @@ qsa_status qsa_select_attention(const void *qa, const void *kcache, const void *
  *   vcache_t    [n_kv_heads][capacity / 64][128][64], same element size, 16-byte aligned;
  *               must not overlap v
  *   capacity    tokens per KV head, a positive multiple of 64
- * Errors: QSA_ERR_INVALID_ARG for NULL or misaligned pointers, n_kv_heads < 1,
- * capacity not a positive multiple of 64, n_kv_heads * capacity >= 2^30, a block
+ * Errors: QSA_ERR_INVALID_ARG for NULL or misaligned pointers, n_kv_heads outside
+ * [1, 65535], capacity not a positive multiple of 64, n_kv_heads * capacity >= 2^30, a block
  * range outside [0, capacity / 64), n_blocks < 0.
  */
 qsa_status qsa_vcache_transpose(const void *v, void *vcache_t, int n_kv_heads, int capacity, int first_block,

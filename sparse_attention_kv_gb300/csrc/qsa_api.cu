@@ -238,6 +238,41 @@ qsa_status qsa_block_topk(const float *scores, int64_t scores_stride, const int3
                     static_cast<cudaStream_t>(stream));
 }
 
+qsa_status qsa_block_candidates(const float *scores, int64_t scores_stride, const int32_t *n_blocks, int nq,
+                                int max_blocks, int active_blocks, int k, int32_t block_offset, float *cand_scores,
+                                int32_t *cand_ids, void *ws, size_t ws_bytes, qsa_path path, qsa_stream stream) {
+    qsa_status st = check_common(nq, max_blocks, active_blocks);
+    if (st != QSA_OK) return st;
+    if (!scores || !n_blocks || !cand_scores || !cand_ids)
+        return fail(QSA_ERR_INVALID_ARG, "NULL scores, n_blocks, cand_scores or cand_ids");
+    if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
+    if (scores_stride < max_blocks)
+        return fail(QSA_ERR_INVALID_ARG, "scores_stride %lld < max_blocks %d", (long long)scores_stride,
+                    max_blocks);
+    if (block_offset < 0 || (long long)block_offset + max_blocks > 0x7fffffffll)
+        return fail(QSA_ERR_INVALID_ARG, "block_offset %d: global ids must lie in [0, 2^31 - 1)", block_offset);
+    st = check_ws(ws, ws_bytes, nq, max_blocks, k);
+    if (st != QSA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = run_topk(scores, scores_stride, n_blocks, nq, max_blocks, active_blocks, k, cand_ids, ws, path, s);
+    if (st != QSA_OK) return st;
+    return launch_candidates(scores, scores_stride, cand_ids, cand_scores, nq, k, block_offset, s);
+}
+
+qsa_status qsa_merge_candidates(const float *cand_scores, const int32_t *cand_ids, int n_shards, int nq, int k,
+                                int32_t *ids, qsa_stream stream) {
+    if (!cand_scores || !cand_ids || !ids) return fail(QSA_ERR_INVALID_ARG, "NULL cand_scores, cand_ids or ids");
+    if (nq < 1) return fail(QSA_ERR_INVALID_ARG, "nq must be >= 1 (got %d)", nq);
+    if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
+    if (n_shards < 1) return fail(QSA_ERR_INVALID_ARG, "n_shards must be >= 1 (got %d)", n_shards);
+    if ((long long)n_shards * k > kMergeCap)
+        return fail(QSA_ERR_UNSUPPORTED, "n_shards x k = %lld candidates per query; the merge holds at most %d",
+                    (long long)n_shards * k, kMergeCap);
+    if ((long long)n_shards * nq * k >= (1ll << 31))
+        return fail(QSA_ERR_INVALID_ARG, "n_shards x nq x k too large");
+    return launch_merge(cand_scores, cand_ids, n_shards, nq, k, ids, static_cast<cudaStream_t>(stream));
+}
+
 qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype dt,
                       const int32_t *n_blocks, int nq, int n_heads, int head_dim, int max_blocks,
                       int active_blocks, int k, int32_t *ids, float *scores,
@@ -336,7 +371,8 @@ qsa_status qsa_vcache_transpose(const void *v, void *vcache_t, int n_kv_heads, i
     if (!v || !vcache_t) return fail(QSA_ERR_INVALID_ARG, "NULL v or vcache_t");
     if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(vcache_t)) & 15u)
         return fail(QSA_ERR_INVALID_ARG, "v and vcache_t must be 16-byte aligned");
-    if (n_kv_heads < 1) return fail(QSA_ERR_INVALID_ARG, "n_kv_heads must be >= 1 (got %d)", n_kv_heads);
+    if (n_kv_heads < 1 || n_kv_heads > 65535)   // one grid row per KV head
+        return fail(QSA_ERR_INVALID_ARG, "n_kv_heads must be in [1, 65535] (got %d)", n_kv_heads);
     if (capacity < 64 || capacity % 64)
         return fail(QSA_ERR_INVALID_ARG, "capacity must be a positive multiple of 64 (got %d)", capacity);
     if ((long long)n_kv_heads * capacity >= (1ll << 30))

@@ -34,6 +34,8 @@ constexpr int kRegisterCap = 8192;
 constexpr int kSplitSlots = 4096;
 // Largest chunk of the split's stage A (256 threads x 4 keys).
 constexpr int kSplitMaxChunk = 1024;
+// Candidates per query the merge of sharded selections holds on chip (shards x k).
+constexpr int kMergeCap = 4096;
 
 // Workspace layout; every region starts on a 256-byte boundary.
 struct WsLayout {
@@ -79,6 +81,13 @@ qsa_status launch_topk_sample(const TopkArgs &a, cudaStream_t s);
 // CTAs are launched early and wait on the SMs the scorer leaves free)
 qsa_status launch_topk_warp(const TopkArgs &a, bool behind_scorer, cudaStream_t s);
 qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t s);
+
+// Sharded selection: the candidates' scores and global ids after a shard's top-k
+// (ids [nq][k] in place), and the merge of [n_shards][nq][k] candidates into ids.
+qsa_status launch_candidates(const float *scores, int64_t stride, int32_t *ids, float *cand_scores, int nq, int k,
+                             int32_t offset, cudaStream_t s);
+qsa_status launch_merge(const float *cand_scores, const int32_t *cand_ids, int n_shards, int nq, int k, int32_t *ids,
+                        cudaStream_t s);
 
 struct ScorerArgs {
     const void *q;

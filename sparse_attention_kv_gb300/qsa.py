@@ -34,8 +34,10 @@ ATTN_GROUP = 16
 ATTN_MAX_K = 64
 
 EXPORTS = ("qsa_workspace_bytes", "qsa_workspace_init", "qsa_block_scores", "qsa_block_topk",
-           "qsa_block_topk_static", "qsa_select", "qsa_select_attention", "qsa_vcache_transpose", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
+           "qsa_block_topk_static", "qsa_block_candidates", "qsa_merge_candidates", "qsa_select",
+           "qsa_select_attention", "qsa_vcache_transpose", "qsa_read_flags", "qsa_auto_path", "qsa_last_error",
            "qsa_version")
+MERGE_CAP = 4096   # candidates per query qsa_merge_candidates holds (n_shards x k)
 
 
 class QSAError(RuntimeError):
@@ -68,6 +70,10 @@ def load() -> ctypes.CDLL:
     lib.qsa_block_topk.restype = i32
     lib.qsa_block_topk_static.argtypes = [vp, i64, vp, i32, i32, i32, i32, vp, i32, vp]
     lib.qsa_block_topk_static.restype = i32
+    lib.qsa_block_candidates.argtypes = [vp, i64, vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, i32, vp]
+    lib.qsa_block_candidates.restype = i32
+    lib.qsa_merge_candidates.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+    lib.qsa_merge_candidates.restype = i32
     lib.qsa_select.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, i64, i32, vp,
                                sz, i32, vp]
     lib.qsa_select.restype = i32
@@ -199,6 +205,46 @@ def block_topk_static(scores: torch.Tensor, n_blocks: torch.Tensor, k: int, ids:
     st = lib.qsa_block_topk_static(_dptr(scores, "scores"), scores.stride(0), _dptr(n_blocks, "n_blocks"), nq,
                                    mb, active_blocks, k, _dptr(ids, "ids"), path, _stream(stream))
     _check("qsa_block_topk_static", st)
+    return ids
+
+
+def block_candidates(scores: torch.Tensor, n_blocks: torch.Tensor, k: int, cand_scores: torch.Tensor,
+                     cand_ids: torch.Tensor, ws: torch.Tensor, block_offset: int, max_blocks: int | None = None,
+                     active_blocks: int = -1, path: int = PATH_AUTO, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """One shard's candidates: cand_ids [nq, k] (global ids = block_offset + local id,
+    ascending, -1 padded) and cand_scores [nq, k] fp32, over scores [nq, >= max_blocks]."""
+    lib = load()
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be a 2-D fp32 tensor with unit inner stride")
+    nq = scores.shape[0]
+    if cand_ids.dtype != torch.int32 or not cand_ids.is_contiguous() or tuple(cand_ids.shape) != (nq, k):
+        raise ValueError("cand_ids must be a contiguous int32 tensor [nq, k]")
+    if cand_scores.dtype != torch.float32 or not cand_scores.is_contiguous() or tuple(cand_scores.shape) != (nq, k):
+        raise ValueError("cand_scores must be a contiguous fp32 tensor [nq, k]")
+    _contig(n_blocks, "n_blocks")
+    mb = scores.shape[1] if max_blocks is None else max_blocks
+    st = lib.qsa_block_candidates(_dptr(scores, "scores"), scores.stride(0), _dptr(n_blocks, "n_blocks"), nq, mb,
+                                  active_blocks, k, int(block_offset), _dptr(cand_scores, "cand_scores"),
+                                  _dptr(cand_ids, "cand_ids"), _dptr(ws, "ws"), ws.numel(), path, _stream(stream))
+    _check("qsa_block_candidates", st)
+    return cand_scores, cand_ids
+
+
+def merge_candidates(cand_scores: torch.Tensor, cand_ids: torch.Tensor, ids: torch.Tensor,
+                     stream=None) -> torch.Tensor:
+    """ids [nq, k] (ascending, -1 padded) selected over every shard's candidates
+    cand_scores / cand_ids [n_shards, nq, k]."""
+    lib = load()
+    if cand_scores.dim() != 3 or cand_scores.dtype != torch.float32 or not cand_scores.is_contiguous():
+        raise ValueError("cand_scores must be a contiguous fp32 tensor [n_shards, nq, k]")
+    if cand_ids.dtype != torch.int32 or not cand_ids.is_contiguous() or cand_ids.shape != cand_scores.shape:
+        raise ValueError("cand_ids must be a contiguous int32 tensor shaped like cand_scores")
+    G, nq, k = cand_scores.shape
+    if ids.dtype != torch.int32 or not ids.is_contiguous() or tuple(ids.shape) != (nq, k):
+        raise ValueError("ids must be a contiguous int32 tensor [nq, k]")
+    st = lib.qsa_merge_candidates(_dptr(cand_scores, "cand_scores"), _dptr(cand_ids, "cand_ids"), G, nq, k,
+                                  _dptr(ids, "ids"), _stream(stream))
+    _check("qsa_merge_candidates", st)
     return ids
 
 

@@ -133,7 +133,8 @@ def test_select_attention_rejects_bad_arguments_before_launch(lib, case, status)
 
 @pytest.mark.parametrize("case", [
     dict(v=None), dict(v=FAKE + 2), dict(n_kv=0), dict(capacity=100), dict(capacity=0),
-    dict(first=-1), dict(n=-1), dict(first=60, n=5), dict(vt=FAKE + 4096),   # the last: overlapping buffers
+    dict(first=-1), dict(n=-1), dict(first=60, n=5), dict(vt=FAKE + 4096),   # overlapping buffers
+    dict(n_kv=70000, capacity=64, n=1),   # more KV heads than a grid dimension holds
 ])
 def test_vcache_transpose_rejects_bad_arguments(lib, case):
     a = dict(v=FAKE, vt=FAKE + (1 << 24), n_kv=2, capacity=4096, first=0, n=64)
@@ -152,6 +153,70 @@ def test_topk_rejects_bad_arguments_before_launch(lib):
     assert st == qsa.ERR_INVALID_ARG
     st = lib.qsa_block_topk(FAKE, 1024, FAKE, 4, 1024, -1, 32, FAKE, FAKE, 1 << 30, 9, None)
     assert st == qsa.ERR_INVALID_ARG   # bad path enum
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(scores=None), qsa.ERR_INVALID_ARG),
+    (dict(cand_scores=None), qsa.ERR_INVALID_ARG),
+    (dict(cand_ids=None), qsa.ERR_INVALID_ARG),
+    (dict(offset=-1), qsa.ERR_INVALID_ARG),
+    (dict(offset=(1 << 31) - 1000), qsa.ERR_INVALID_ARG),   # ids past 2^31 - 1
+    (dict(k=0), qsa.ERR_INVALID_ARG),
+    (dict(k=1025), qsa.ERR_INVALID_ARG),
+    (dict(nq=0), qsa.ERR_INVALID_ARG),
+    (dict(stride=100), qsa.ERR_INVALID_ARG),
+    (dict(active=-2), qsa.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), qsa.ERR_WORKSPACE),
+    (dict(ws=None), qsa.ERR_WORKSPACE),
+    (dict(path=9), qsa.ERR_INVALID_ARG),
+])
+def test_block_candidates_rejects_bad_arguments_before_launch(lib, case, status):
+    a = dict(scores=FAKE, stride=1024, n_blocks=FAKE, nq=4, max_blocks=1024, active=-1, k=32, offset=4096,
+             cand_scores=FAKE, cand_ids=FAKE, ws=FAKE, ws_bytes=1 << 30, path=qsa.PATH_AUTO)
+    a.update(case)
+    st = lib.qsa_block_candidates(a["scores"], a["stride"], a["n_blocks"], a["nq"], a["max_blocks"], a["active"],
+                                  a["k"], a["offset"], a["cand_scores"], a["cand_ids"], a["ws"], a["ws_bytes"],
+                                  a["path"], None)
+    assert st == status
+    assert lib.qsa_last_error().decode()
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(cs=None), qsa.ERR_INVALID_ARG),
+    (dict(ci=None), qsa.ERR_INVALID_ARG),
+    (dict(ids=None), qsa.ERR_INVALID_ARG),
+    (dict(nq=0), qsa.ERR_INVALID_ARG),
+    (dict(k=0), qsa.ERR_INVALID_ARG),
+    (dict(k=1025), qsa.ERR_INVALID_ARG),
+    (dict(g=0), qsa.ERR_INVALID_ARG),
+    (dict(g=129, k=32), qsa.ERR_UNSUPPORTED),   # 4,128 candidates per query
+    (dict(g=5, k=1024), qsa.ERR_UNSUPPORTED),
+])
+def test_merge_candidates_rejects_bad_arguments_before_launch(lib, case, status):
+    a = dict(cs=FAKE, ci=FAKE, g=4, nq=8, k=32, ids=FAKE)
+    a.update(case)
+    st = lib.qsa_merge_candidates(a["cs"], a["ci"], a["g"], a["nq"], a["k"], a["ids"], None)
+    assert st == status
+    assert lib.qsa_last_error().decode()
+
+
+def test_merge_capacity_matches_binding(lib):
+    assert lib.qsa_merge_candidates(FAKE, FAKE, qsa.MERGE_CAP // 32 + 1, 1, 32, FAKE, None) == qsa.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 1024, FAKE, 4, 1024, -1, 32, FAKE, 0), qsa.ERR_INVALID_ARG),
+    ((FAKE, 100, FAKE, 4, 1024, -1, 32, FAKE, 0), qsa.ERR_INVALID_ARG),      # stride < max_blocks
+    ((FAKE, 1024, FAKE, 4, 1024, -2, 32, FAKE, 0), qsa.ERR_INVALID_ARG),
+    ((FAKE, 1024, FAKE, 4, 1024, -1, 32, FAKE, 9), qsa.ERR_INVALID_ARG),     # bad path
+    ((FAKE, 1024, None, 4, 1024, -1, 32, FAKE, 0), qsa.ERR_INVALID_ARG),
+    ((FAKE, 8192, FAKE, 256, 8192, -1, 1024, FAKE, 0), qsa.ERR_WORKSPACE),  # beyond the static scratch
+])
+def test_static_topk_rejects_before_touching_its_scratch(lib, args, status):
+    """Rejected calls return before the scratch is looked up or cleared (no CUDA call
+    at all, so this runs without a GPU)."""
+    assert lib.qsa_block_topk_static(*args, None) == status
+    assert lib.qsa_last_error().decode()
 
 
 def test_binding_raises_when_library_missing(monkeypatch, tmp_path):

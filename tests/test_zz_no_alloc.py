@@ -4,7 +4,8 @@ Callers that may not allocate device memory where they select blocks -- a fixed
 arena that must not grow, a plug-in given only its input and output buffers --
 use qsa_block_topk_static, which takes its scratch from an array compiled into
 the library.  Its ids must equal those of qsa_block_topk (the caller-workspace
-entry point) bit for bit, on consecutive calls that reuse the shared scratch.
+entry point) bit for bit, and the oracle's selection over the same scores, on
+consecutive calls that reuse the shared scratch.
 This file is collected last, so a run that stops at its first failure has run
 every other test before it.
 """
@@ -13,6 +14,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from sparse_attention_kv_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +34,7 @@ def _call_static(lib, scores, n_dev, k, ids, max_blocks, active, path):
 
 
 @pytest.mark.parametrize("shape", [
-    (3, 4096, [4032, 626, 4096], 32, -1, qsa.PATH_AUTO),        # decode window: the split path
+    (3, 4096, [4032, 626, 4096], 32, -1, qsa.PATH_AUTO),        # decode window: the warp path
     (3, 4096, [4032, 4000, 31], 32, -1, qsa.PATH_SPLIT),
     (128, 2048, None, 32, 2048, qsa.PATH_SAMPLE),               # prompt rows: sampled filter
     (16, 8192, None, 64, 8192, qsa.PATH_RADIX),
@@ -54,6 +56,8 @@ def test_static_entry_matches_workspace_entry_on_two_calls(shape):
         assert st == qsa.OK, lib.qsa_last_error().decode()
         torch.cuda.synchronize()
         np.testing.assert_array_equal(got.cpu().numpy(), want.cpu().numpy())
+        # and both are the oracle's selection over the same scores
+        np.testing.assert_array_equal(got.cpu().numpy(), oracle.select_f32(sc, nb, k))
 
 
 def test_static_entry_rejects_sizes_beyond_its_scratch():
