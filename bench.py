@@ -40,7 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from sparse_attention_kv_gb300 import inputs  # noqa: E402
+from workloads import inputs  # noqa: E402
 
 METRIC = "us per select call (score+top-k), 256q x 520K tokens"
 UNIT = "us/call"
@@ -361,18 +361,78 @@ def attention_report(acase, adcase, us, us_dec, peaks, peak_src):
     }
 
 
-def warm_us_per_call(torch, fn, calls, stream):
-    """Back-to-back calls between one event pair (no flush): steady-state us per call."""
-    fn()
+def us_mean(times_ms):
+    """Mean of per-call event times, in us.  The event timer's resolution is coarse on
+    this GPU (about 2 us steps), so the mean over many calls is reported, not the
+    median, which snaps to the step."""
+    return statistics.mean(times_ms) * 1e3
+
+
+def graph_us_per_call(torch, fns, replays=5):
+    """Device time per call of the calls ``fns`` captured in one CUDA graph and replayed
+    back to back: no host launch between them and no L2 flush, so a kernel whose inputs
+    rotate through more memory than L2 holds still reads them from DRAM.  Events
+    around each replay; mean over the replays, divided by the calls."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    st = torch.cuda.Event(enable_timing=True)
-    en = torch.cuda.Event(enable_timing=True)
-    st.record(stream)
-    for _ in range(calls):
-        fn()
-    en.record(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for f in fns:
+            f()
+    g.replay()
     torch.cuda.synchronize()
-    return st.elapsed_time(en) * 1e3 / calls
+    ts = []
+    for _ in range(replays):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts) * 1e3 / len(fns)
+
+
+def oracle_scores(case, rows=None):
+    """FP64 oracle scores of the case's queries ``rows`` (all by default), over every
+    host core (the oracle's C calls release the GIL)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.build()
+    rows = np.arange(case.nq) if rows is None else np.asarray(rows)
+    chunks = [rows[i:i + 8] for i in range(0, len(rows), 8)]
+    with ThreadPoolExecutor(os.cpu_count() or 1) as ex:
+        parts = list(ex.map(lambda r: oracle.block_scores(case.q[r], case.w[r], case.kblk, case.n_blocks[r],
+                                                          case.dtype), chunks))
+    return np.concatenate(parts, axis=0)
+
+
+def parity_report(case, gpu_scores, chained_ids, timed_ids, form):
+    """Rules (a)-(c) on a timed workload, through the oracle, outside any timed region:
+    (a) the chained call's ids against the oracle's selection over the GPU's own scores,
+    (b) the GPU's scores against the FP64 oracle, (c) the timed form's ids against the
+    oracle's FP64 selection, with the near-tie counts at the tolerance and at four times
+    the observed score error."""
+    import oracle
+    from oracle import parity
+    ref = oracle_scores(case)
+    n = case.n_blocks
+    err = parity.score_errors(gpu_scores, ref, n)
+    a_ids = oracle.select_f32(gpu_scores, n, case.k)
+    a_same = int((chained_ids == a_ids).all(1).sum())
+    tol = parity.TOL[case.dtype]
+    tight = max(4.0 * float(err.max()), 1e-9)
+    rc = parity.rule_c(timed_ids, ref, oracle.select(ref, n, case.k), n, case.k, tol, tight)
+    rc.pop("failed_ids")
+    return {"workload": case.name, "queries": case.nq,
+            "rule_a": {"identical_queries": a_same, "pass": a_same == case.nq},
+            "rule_b": {"max_normalised_error": float(err.max()), "tol": tol, "pass": bool(err.max() <= tol)},
+            "rule_c": dict(rc, form=form, tol=tol, tight_tol=tight, **{"pass": rc["failed"] == 0})}
 
 
 def run_ours(args):
@@ -384,12 +444,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     from sparse_attention_kv_gb300 import qsa
-    from tests import parity
+    from workloads import device
     qsa.load()
     stream = torch.cuda.current_stream()
 
     case = inputs.deep_case(2)
-    q, w, kb, nb = parity.to_device(case, dev)
+    q, w, kb, nb = device.to_device(case, dev)
     C = case.max_blocks
     n = int(case.n_blocks[0])
     scores = torch.empty((case.nq, C), dtype=torch.float32, device=dev)
@@ -419,7 +479,7 @@ def run_ours(args):
 
     # decode window, 3 queries at 258,000 tokens
     dcase = inputs.decode_case(5)
-    dq, dw, dkb, dnb = parity.to_device(dcase, dev)
+    dq, dw, dkb, dnb = device.to_device(dcase, dev)
     dscores = torch.empty((dcase.nq, dcase.max_blocks), dtype=torch.float32, device=dev)
     dids = torch.empty((dcase.nq, dcase.k), dtype=torch.int32, device=dev)
     dws = qsa.alloc_workspace(dcase.nq, dcase.max_blocks, dcase.k, device=dev)
@@ -469,17 +529,17 @@ def run_ours(args):
     decode_chained()
     torch.cuda.synchronize()
     acase = inputs.deep_attention_case(ids=ids.cpu().numpy())
-    a_dev = parity.attn_to_device(acase, dev)
+    a_dev = device.attn_to_device(acase, dev)
     a_out = torch.empty((acase.nq, acase.n_heads, 128), dtype=torch.float32, device=dev)
     a_lse = torch.empty((acase.nq, acase.n_heads), dtype=torch.float32, device=dev)
     adcase = inputs.decode_attention_case(ids=dids.cpu().numpy())
-    ad_dev = parity.attn_to_device(adcase, dev)
+    ad_dev = device.attn_to_device(adcase, dev)
     ad_out = torch.empty((adcase.nq, adcase.n_heads, 128), dtype=torch.float32, device=dev)
     ad_lse = torch.empty((adcase.nq, adcase.n_heads), dtype=torch.float32, device=dev)
 
     # the prompt call: 256 queries at 131,072 tokens
     pcase = inputs.prompt_case()
-    pq, pw, pkb, pnb = parity.to_device(pcase, dev)
+    pq, pw, pkb, pnb = device.to_device(pcase, dev)
     pscores = torch.empty((pcase.nq, pcase.max_blocks), dtype=torch.float32, device=dev)
     pids = torch.empty((pcase.nq, pcase.k), dtype=torch.int32, device=dev)
     pws = qsa.alloc_workspace(pcase.nq, pcase.max_blocks, pcase.k, fused=True, device=dev)
@@ -495,7 +555,7 @@ def run_ours(args):
 
     # the deep prompt with fp8 e4m3 queries and keys
     ecase = inputs.deep_e4m3_case()
-    eq, ew, ekb, enb = parity.to_device(ecase, dev)
+    eq, ew, ekb, enb = device.to_device(ecase, dev)
     escores = torch.empty((ecase.nq, ecase.max_blocks), dtype=torch.float32, device=dev)
     eids = torch.empty((ecase.nq, ecase.k), dtype=torch.int32, device=dev)
     ews = qsa.alloc_workspace(ecase.nq, ecase.max_blocks, ecase.k, fused=True, device=dev)
@@ -543,7 +603,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     # qsa_select has two forms (one fused kernel, or scorer then top-k); the faster
     # one on this GPU is the call a user makes, and is the one timed below
-    probe = {f: statistics.median(timed_loop(torch, fn, 30, flush, stream))
+    probe = {f: statistics.mean(timed_loop(torch, fn, 30, flush, stream))
              for f, fn in (("fused", select_fused), ("chained", select_chained))}
     form = min(probe, key=probe.get)
     select = select_fused if form == "fused" else select_chained
@@ -605,24 +665,54 @@ def run_ours(args):
                 fn()
             except qsa.QSAError:
                 continue
-            res[qsa.PATH_NAMES[pth]] = statistics.median(timed_loop(torch, fn, 50, flush, stream)) * 1e3
+            res[qsa.PATH_NAMES[pth]] = us_mean(timed_loop(torch, fn, 100, flush, stream))
         topk_paths[name] = res
-    warm = {"deep_chained": warm_us_per_call(torch, select_chained, 200, stream),
-            "deep_fused": warm_us_per_call(torch, select_fused, 200, stream),
-            "decode_chained": warm_us_per_call(torch, decode_chained, 200, stream),
-            "decode_fused": warm_us_per_call(torch, decode_fused, 200, stream)}
+    # device time per call with no host launch in between (one CUDA graph of calls back
+    # to back): the top-k over 24 copies of the deep scores (200 MB, more than L2 holds,
+    # so each call reads its rows from DRAM), the scorer, and both select forms
+    select_chained()
+    torch.cuda.synchronize()
+    rot = [scores.clone() for _ in range(24)]
+    graph_us = {
+        "topk_deep_rotating_scores": graph_us_per_call(
+            torch, [lambda r_=r_: qsa.block_topk(r_, nb, case.k, ids, ws, active_blocks=case.active_blocks)
+                    for r_ in rot]),
+        "scorer_deep": graph_us_per_call(torch, [score_only] * 20),
+        "select_deep_chained": graph_us_per_call(torch, [select_chained] * 20),
+        "select_deep_fused": graph_us_per_call(torch, [select_fused] * 20),
+        "select_decode_chained": graph_us_per_call(torch, [decode_chained] * 20),
+        "select_decode_fused": graph_us_per_call(torch, [decode_fused] * 20)}
+    del rot
     clocks = sampler.stop()
 
     ms_main = max_over_ranks(statistics.mean(t_main), device=dev)
     if rank != 0:
         return 0
 
+    # rules (a)-(c) on the timed workloads through the oracle, outside every timed region
+    parity = None
+    if not args.no_parity:
+        select_chained()
+        torch.cuda.synchronize()
+        chained_ids = ids.cpu().numpy().copy()
+        gpu_scores = scores.cpu().numpy()
+        select()
+        torch.cuda.synchronize()
+        parity = {"deep": parity_report(case, gpu_scores, chained_ids, ids.cpu().numpy(), form)}
+        decode_chained()
+        torch.cuda.synchronize()
+        dch = dids.cpu().numpy().copy()
+        dsc = dscores.cpu().numpy()
+        decode_fused()
+        torch.cuda.synchronize()
+        parity["decode"] = parity_report(dcase, dsc, dch, dids.cpu().numpy(), "fused")
+
     peaks, peak_src = load_peaks()
     us_main = job_us_per_call(ms_main, world)
-    us_main_median = statistics.median(t_main) * 1e3
-    us_other = statistics.median(t_other) * 1e3
-    us_score = statistics.median(t_score) * 1e3
-    us_topk = statistics.median(t_topk) * 1e3
+    us_main_mean = us_mean(t_main)
+    us_other = us_mean(t_other)
+    us_score = us_mean(t_score)
+    us_topk = us_mean(t_topk)
     flops = 2.0 * case.nq * case.n_heads * 128 * n
     topk_bytes = 4.0 * case.nq * n + 4.0 * case.nq * case.k + 4.0 * case.nq
     tflops = flops / (us_score * 1e-6) / 1e12
@@ -636,32 +726,44 @@ def run_ours(args):
                  "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                  "traffic": profiled_traffic("topk"), "per_launch": f"{topk_bytes:.4g} B",
                  "us_per_launch": us_topk, "peak_source": f"{peak_src} HBM copy"}
+    # the same kernels' fractions by device time alone (graph replays, no launch or event
+    # overhead per call; the top-k's rows come from DRAM, the scorer's inputs stay in L2)
+    g_topk, g_score = graph_us["topk_deep_rotating_scores"], graph_us["scorer_deep"]
+    topk_roof.update(us_per_launch_graph=g_topk,
+                     frac_kernel=topk_bytes / (g_topk * 1e-6) / 1e9 / peaks["hbm_gbs"])
+    scorer_roof.update(us_per_launch_graph=g_score,
+                       frac_kernel=flops / (g_score * 1e-6) / 1e12 / peaks["bf16_tflops"])
     if form == "fused":
         # one launch per call: the fused kernel is the whole path; its work is the contraction
-        ftf = flops / (us_main_median * 1e-6) / 1e12
+        ftf = flops / (us_main_mean * 1e-6) / 1e12
         roof = {"kernel": "scorer_tc_kernel<bf16, 16, fused>", "bound": "tensor", "achieved": ftf,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ftf / peaks["bf16_tflops"],
                 "traffic": profiled_traffic("fused"),
                 "per_launch": f"{flops:.4g} FLOP (2 x 256 q x 16 h x 128 x {n} blocks), scores kept on chip",
-                "us_per_launch": us_main_median, "peak_source": f"{peak_src} bf16 burst (dense cuBLAS)"}
+                "us_per_launch": us_main_mean, "peak_source": f"{peak_src} bf16 burst (dense cuBLAS)"}
     else:
         roof = scorer_roof if us_score >= us_topk else topk_roof
     dec_n = int(dcase.n_blocks[0])
+    path_bytes = {"deep": topk_bytes, "decode": 4.0 * dcase.nq * dec_n + 4.0 * dcase.nq * dcase.k + 4.0 * dcase.nq}
+    topk_path_table = {w_: {p_: {"us": u_, "gbs": path_bytes[w_] / (u_ * 1e-6) / 1e9,
+                                 "frac": path_bytes[w_] / (u_ * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+                            for p_, u_ in d_.items()}
+                       for w_, d_ in topk_paths.items()}
     dec_bytes = 256.0 * dec_n + 4096.0 * dcase.nq + 64.0 * dcase.nq + 8.0 * dcase.nq * dec_n + 4.0 * dcase.nq * dcase.k
-    us_dec_f = statistics.median(t_dec_f) * 1e3
-    us_dec_c = statistics.median(t_dec_c) * 1e3
+    us_dec_f = us_mean(t_dec_f)
+    us_dec_c = us_mean(t_dec_c)
     us_dec = min(us_dec_f, us_dec_c)
     us_e2e = statistics.mean(t_e2e) * 1e3
-    attn = attention_report(acase, adcase, statistics.median(t_attn) * 1e3, statistics.median(t_attn_dec) * 1e3,
+    attn = attention_report(acase, adcase, us_mean(t_attn), us_mean(t_attn_dec),
                             peaks, peak_src)
     # select then attend in one sequence: the attention launches as the top-k's
     # programmatic dependent (the sum of the two calls timed apart is beside it)
     attn["select_then_attend_us"] = {
-        "deep": statistics.median(t_step["deep"]) * 1e3,
-        "deep_parts_sum": us_main_median + attn["us_per_launch"],
-        "decode": statistics.median(t_step["decode"]) * 1e3,
-        "decode_parts_sum": statistics.median(t_dec_c) * 1e3 + attn["decode"]["us_per_call"]}
-    p_us = {k_: statistics.median(v_) * 1e3 for k_, v_ in t_prompt.items()}
+        "deep": us_mean(t_step["deep"]),
+        "deep_parts_sum": us_main_mean + attn["us_per_launch"],
+        "decode": us_mean(t_step["decode"]),
+        "decode_parts_sum": us_mean(t_dec_c) + attn["decode"]["us_per_call"]}
+    p_us = {k_: us_mean(v_) for k_, v_ in t_prompt.items()}
     p_n = int(pcase.n_blocks[0])
     p_flops = 2.0 * pcase.nq * pcase.n_heads * 128 * p_n
     p_tf = p_flops / (p_us["scorer"] * 1e-6) / 1e12
@@ -669,7 +771,7 @@ def run_ours(args):
               "scorer": {"kernel": "scorer_tc_kernel<bf16, 16>", "us_per_launch": p_us["scorer"],
                          "achieved": p_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": p_tf / peaks["bf16_tflops"], "per_launch": f"{p_flops:.4g} FLOP"}}
-    e_us = {k_: statistics.median(v_) * 1e3 for k_, v_ in t_e4m3.items()}
+    e_us = {k_: us_mean(v_) for k_, v_ in t_e4m3.items()}
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     e_tf = flops / (e_us["scorer"] * 1e-6) / 1e12
     e4m3 = {"workload": ecase.name, "select_us": {"chained": e_us["chained"], "fused": e_us["fused"]},
@@ -688,7 +790,7 @@ def run_ours(args):
                              "launched as its programmatic dependent")),
         "selections_per_s": case.nq * world / (ms_main * 1e-3),
         "roofline": roof,
-        "forms_us_median": {form: us_main_median, ("chained" if form == "fused" else "fused"): us_other},
+        "forms_us_mean": {form: us_main_mean, ("chained" if form == "fused" else "fused"): us_other},
         "scorer": dict(scorer_roof, frac_of_bf16_peak=scorer_roof["frac"]),
         "topk": dict(topk_roof, path=qsa.PATH_NAMES[path], bytes=topk_bytes, l2="cold (flushed)"),
         "decode_3q_258K": {"us_per_call": us_dec, "form": "fused" if us_dec_f <= us_dec_c else "chained",
@@ -701,8 +803,9 @@ def run_ours(args):
         "selection_attention": attn,
         "e4m3_keys": e4m3,
         "prompt_256q_131K": prompt,
-        "topk_paths_us_cold": topk_paths,
-        "warm_back_to_back_us_per_call": warm,
+        "topk_paths_cold": topk_path_table,
+        "graph_us_per_call": graph_us,
+        "parity": parity,
         "gpu_launches": args.steps * (1 if form == "fused" else 1 + topk_launches),
         "clocks": clocks,
         "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"]},
@@ -724,6 +827,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true", help="skip the oracle parity report")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-sample-queries", type=int, default=8)
     ap.add_argument("--profile-steps", type=int, default=0,

@@ -23,6 +23,9 @@ select_attention(qa, kc, vc, ids, n_tokens, scale, dtype)
     selected blocks below its context length, and the log-sum-exp.  ``qa``
     [nq,H,D], ``kc``/``vc`` [Hkv,C,D] (token rows) as bf16 bits (uint16).
 
+The parity rules (a)-(d) that compare the CUDA path's outputs with this
+oracle's are in ``oracle.parity``.
+
 Parity status: pinned (see the oracle tests).
 """
 from __future__ import annotations

@@ -2,7 +2,7 @@
 import numpy as np
 
 import bench
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 
 
 def _case(ids, n_kv=2):
@@ -29,3 +29,22 @@ def test_attention_unique_bytes_count_each_distinct_block_once():
 def test_job_figures_scale_with_the_ranks():
     assert bench.job_us_per_call(0.024, 1) == 24.0
     assert abs(bench.job_us_per_call(0.024, 4) - 6.0) < 1e-12
+
+
+def test_parity_report_on_a_tiny_case_counts_every_query():
+    """The bench's parity block from the oracle's own fp32-rounded scores: rule (a)
+    identical, rule (b) error at fp32 rounding, rule (c) every query exact."""
+    import oracle
+    case = inputs.tiny_case()
+    ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
+    gpu_scores = ref.astype(np.float32)
+    ids = oracle.select_f32(gpu_scores, case.n_blocks, case.k)
+    rep = bench.parity_report(case, gpu_scores, ids, ids, "chained")
+    assert rep["rule_a"] == {"identical_queries": case.nq, "pass": True}
+    assert rep["rule_b"]["pass"] and rep["rule_b"]["max_normalised_error"] < 1e-6
+    assert rep["rule_c"]["pass"] and rep["rule_c"]["exact"] == case.nq and rep["rule_c"]["failed"] == 0
+
+
+def test_event_times_are_averaged_not_snapped():
+    # four calls timed at the ~2 us steps of the event timer (ms in, us out): the mean, not the median
+    assert abs(bench.us_mean([0.002048, 0.002048, 0.004096, 0.002048]) - 2.56) < 1e-9

@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
     try:
         import bench
         import oracle
-        from sparse_attention_kv_gb300 import inputs
+        from workloads import inputs
         mx = bench.max_over_ranks(1.5 + rank)
         # this rank's shard of queries, selected on its own
         sc = inputs.normal_scores(42, 8, 300).astype(np.float64)
@@ -52,7 +52,7 @@ def test_two_gloo_ranks_max_and_query_shards():
     out = mp.Manager().dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     import oracle
-    from sparse_attention_kv_gb300 import inputs
+    from workloads import inputs
     sc = inputs.normal_scores(42, 8, 300).astype(np.float64)
     nb = np.array([300, 299, 120, 40, 3, 300, 255, 1], dtype=np.int32)
     want = oracle.select(sc, nb, 16).tolist()
@@ -93,7 +93,8 @@ def _sharded_worker(rank, world, port, bounds, kind, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
     try:
-        from sparse_attention_kv_gb300 import inputs, sharded
+        from sparse_attention_kv_gb300 import sharded
+        from workloads import inputs
         sc, nb, k = _sharded_case(kind)
         lo, hi = bounds[rank], bounds[rank + 1]
         local = torch.from_numpy(np.ascontiguousarray(sc[:, lo:hi]))
@@ -107,7 +108,7 @@ def _sharded_worker(rank, world, port, bounds, kind, out):
 
 
 def _sharded_case(kind):
-    from sparse_attention_kv_gb300 import inputs
+    from workloads import inputs
     if kind == "normal":
         sc = inputs.normal_scores(4242, 12, 500)
     else:

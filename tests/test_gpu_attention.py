@@ -11,7 +11,7 @@ groups, 520,000 tokens, k = 32) is checked on sampled queries.
 import numpy as np
 import pytest
 
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 
 from .parity import attn_to_device, attention_reference, check_rule_d, to_device
 

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 from tests import parity
 
 pytestmark = pytest.mark.gpu

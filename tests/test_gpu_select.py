@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -102,9 +102,11 @@ def test_e4m3_decode_window_chained_and_fused(fused):
     ref = oracle.block_scores(case.q, case.w, case.kblk, case.n_blocks, case.dtype)
     ids, sc, flags = run_select(case, fused=fused)
     assert flags & qsa.ERROR_FLAGS == 0
-    parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
+    err = parity.check_rule_b(sc, ref, case.n_blocks, case.dtype)
+    assert err <= 1e-5, f"e4m3 products are exact in fp32: error {err:.2e} is above fp32 rounding"
     parity.check_rule_a(ids, oracle.select_f32(sc, case.n_blocks, case.k))
-    parity.check_rule_c(ids, ref, oracle.select(ref, case.n_blocks, case.k), case.n_blocks, case.k, case.dtype)
+    r = parity.check_rule_c(ids, ref, oracle.select(ref, case.n_blocks, case.k), case.n_blocks, case.k, case.dtype)
+    assert r["excused"] == 0 and r["exact"] == case.nq
 
 
 def test_e4m3_deep_prompt_sampled():
@@ -120,9 +122,12 @@ def test_e4m3_deep_prompt_sampled():
     sub = inputs.Case(q=case.q[rows], w=case.w[rows], kblk=case.kblk, n_blocks=case.n_blocks[rows],
                       tokens=case.tokens[rows], dtype=case.dtype, k=case.k, active_blocks=case.active_blocks)
     ref = oracle.block_scores(sub.q, sub.w, sub.kblk, sub.n_blocks, sub.dtype)
-    parity.check_rule_b(sc[rows], ref, sub.n_blocks, sub.dtype)
+    err = parity.check_rule_b(sc[rows], ref, sub.n_blocks, sub.dtype)
+    assert err <= 1e-5, f"e4m3 products are exact in fp32: error {err:.2e} is above fp32 rounding"
     parity.check_rule_a(ids[rows], oracle.select_f32(sc[rows], sub.n_blocks, sub.k))
-    parity.check_rule_c(ids[rows], ref, oracle.select(ref, sub.n_blocks, sub.k), sub.n_blocks, sub.k, sub.dtype)
+    r = parity.check_rule_c(ids[rows], ref, oracle.select(ref, sub.n_blocks, sub.k), sub.n_blocks, sub.k,
+                            sub.dtype)
+    assert r["excused"] == 0 and r["exact"] == len(rows)
 
 
 @pytest.mark.parametrize("H", [1, 2, 4, 8, 16])

@@ -2,7 +2,7 @@
 import numpy as np
 import pytest
 
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 
 
 def test_bf16_rounding_nearest_even():

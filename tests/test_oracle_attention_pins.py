@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import oracle
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 
 bf16 = inputs.to_bf16_bits
 

@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 
 import oracle
-from sparse_attention_kv_gb300 import inputs
+from workloads import inputs
 
 
 def _load(golden_dir, name):
