@@ -100,9 +100,10 @@ typedef void *qsa_stream; /* a cudaStream_t */
 #define QSA_ATTN_MAX_K 64
 
 /*
- * Workspace size in bytes for calls with these sizes (any path, fused or not).
- * A workspace sized for (nq, max_blocks, k) serves every call with sizes at or
- * below these.  The workspace must be zero-filled before its first use (e.g. by
+ * Workspace size in bytes for calls with these sizes: fused != 0 for the fused
+ * form of qsa_select (its per-CTA candidate lists take up to 4,096 entries per
+ * query), else any other call.  A workspace sized for (nq, max_blocks, k, fused)
+ * serves every call with sizes at or below these.  The workspace must be zero-filled before its first use (e.g. by
  * qsa_workspace_init); every call leaves it in a reusable state.  Returns 0 for
  * invalid sizes.
  */

@@ -1,5 +1,6 @@
 // qsa_api.cu -- the C ABI of libqsa.so: argument checks, workspace layout,
 // top-k path dispatch, and the chained select.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -41,9 +42,10 @@ int num_sms() {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-WsLayout ws_layout(int nq, int max_blocks, int k) {
+WsLayout ws_layout(int nq, int max_blocks, int k, bool fused) {
     WsLayout L{};
     L.maxch = (max_blocks + kMinChunk - 1) / kMinChunk;
+    const size_t per_query = std::max<size_t>((size_t)L.maxch * k, fused ? (size_t)kMergeCap : 0);
     size_t off = 0;
     L.flags = off;
     off += 256;
@@ -54,9 +56,9 @@ WsLayout ws_layout(int nq, int max_blocks, int k) {
     L.counts = off;
     off += align256(sizeof(int32_t) * (size_t)nq * L.maxch);
     L.ckeys = off;
-    off += align256(sizeof(uint32_t) * (size_t)nq * L.maxch * k);
+    off += align256(sizeof(uint32_t) * (size_t)nq * per_query);
     L.cids = off;
-    off += align256(sizeof(int32_t) * (size_t)nq * L.maxch * k);
+    off += align256(sizeof(int32_t) * (size_t)nq * per_query);
     L.total = off;
     return L;
 }
@@ -98,11 +100,11 @@ static qsa_status check_common(int nq, int max_blocks, int active_blocks) {
     return QSA_OK;
 }
 
-static qsa_status check_ws(void *ws, size_t ws_bytes, int nq, int max_blocks, int k) {
+static qsa_status check_ws(void *ws, size_t ws_bytes, int nq, int max_blocks, int k, bool fused = false) {
     if (!ws) return fail(QSA_ERR_WORKSPACE, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(ws) & 255u)
         return fail(QSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-    const size_t need = ws_layout(nq, max_blocks, k).total;
+    const size_t need = ws_layout(nq, max_blocks, k, fused).total;
     if (ws_bytes < need)
         return fail(QSA_ERR_WORKSPACE, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
     return QSA_OK;
@@ -186,9 +188,8 @@ using namespace qsa;
 extern "C" {
 
 size_t qsa_workspace_bytes(int nq, int max_blocks, int k, int fused) {
-    (void)fused;
     if (nq < 1 || max_blocks < 1 || max_blocks > QSA_MAX_BLOCKS || k < 1 || k > QSA_MAX_K) return 0;
-    return ws_layout(nq, max_blocks, k).total;
+    return ws_layout(nq, max_blocks, k, fused != 0).total;
 }
 
 qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream) {
@@ -270,7 +271,7 @@ qsa_status qsa_merge_candidates(const float *cand_scores, const int32_t *cand_id
                     (long long)n_shards * k, kMergeCap);
     if ((long long)n_shards * nq * k >= (1ll << 31))
         return fail(QSA_ERR_INVALID_ARG, "n_shards x nq x k too large");
-    return launch_merge(cand_scores, cand_ids, n_shards, nq, k, ids, static_cast<cudaStream_t>(stream));
+    return launch_merge(cand_scores, cand_ids, nullptr, 0, n_shards, nq, k, k, ids, static_cast<cudaStream_t>(stream));
 }
 
 qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype dt,
@@ -283,13 +284,13 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
     if (st != QSA_OK) return st;
     if (!ids) return fail(QSA_ERR_INVALID_ARG, "ids is NULL");
     if (k < 1 || k > QSA_MAX_K) return fail(QSA_ERR_INVALID_ARG, "k must be in [1, %d] (got %d)", QSA_MAX_K, k);
-    st = check_ws(ws, ws_bytes, nq, max_blocks, k);
+    st = check_ws(ws, ws_bytes, nq, max_blocks, k, fused != 0);
     if (st != QSA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fused) {
         if (path != QSA_PATH_AUTO)
             return fail(QSA_ERR_UNSUPPORTED, "fused score-then-select has no top-k path to force (got %d)", (int)path);
-        const WsLayout L = ws_layout(nq, max_blocks, k);
+        const WsLayout L = ws_layout(nq, max_blocks, k, true);
         char *base = static_cast<char *>(ws);
         ScorerArgs a{};
         a.q = q;
@@ -307,10 +308,9 @@ qsa_status qsa_select(const void *q, const float *w, const void *kblk, qsa_dtype
         a.fused = true;
         a.ids = ids;
         a.k = k;
-        a.tickets = reinterpret_cast<uint32_t *>(base + L.tickets);
-        // 8 bytes per candidate fit in the two 4-byte candidate arrays, which are adjacent
-        static_assert(sizeof(uint64_t) == 2 * sizeof(uint32_t), "packed candidate size");
-        a.cand = reinterpret_cast<uint64_t *>(base + L.ckeys);
+        a.cand_scores = reinterpret_cast<float *>(base + L.ckeys);
+        a.cand_ids = reinterpret_cast<int32_t *>(base + L.cids);
+        a.counts = reinterpret_cast<int32_t *>(base + L.counts);
         a.maxch = L.maxch;
         return launch_scorer(a, s);
     }

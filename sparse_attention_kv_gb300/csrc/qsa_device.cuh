@@ -21,6 +21,11 @@ __device__ __forceinline__ uint32_t score_key(float x) {
     return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
+// Inverse of score_key (for keys of non-NaN scores; both zeros come back as +0).
+__device__ __forceinline__ float key_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
 // Programmatic dependent launch.  wait_prior_grid() blocks until the grid launched
 // before this one on the stream has completed and its memory writes are visible; it
 // returns at once when this grid was launched without the programmatic attribute.
@@ -565,6 +570,50 @@ __device__ __forceinline__ void warp_rank_top(uint64_t *buf, int m, int k, Emit 
     if (lane < m && r0 < k) emit(r0, v0);
     if (lane + 32 < m && r1 < k) emit(r1, v1);
     __syncwarp();
+}
+
+// Exact ranks of m distinct packed candidates cand[0..m) (rank 0 = the largest):
+// sel[r] = the id of the candidate of rank r, for r < k (exactly k rank below k when
+// m >= k).  A rank is the number of candidates above; P threads per candidate (a
+// power of two dividing the warp) share the count.  Every thread of the NT-thread
+// block calls it.
+template <int NT>
+__device__ __forceinline__ void rank_survivors(const uint64_t *cand, int m, int k, int32_t *sel) {
+    if (m <= 64) {   // the common case: every compare unrolled, P fixed
+        constexpr int P = NT / 64;
+        const int i = (int)threadIdx.x / P, sub = (int)threadIdx.x % P;
+        const uint64_t c = i < m ? cand[i] : 0ull;
+        int rk = 0;
+#pragma unroll
+        for (int t = 0; t < 64 / P; ++t) {
+            const int j = sub + P * t;
+            rk += j < m && cand[j] > c;
+        }
+#pragma unroll
+        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
+        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
+        return;
+    }
+    int lp = 0;   // P = 1 << lp <= 8, as many as the block holds
+    while (lp < 3 && (2 * m << lp) <= NT) ++lp;
+    const int P = 1 << lp;
+    for (int b0 = 0; b0 < m * P; b0 += NT) {
+        const int e = b0 + (int)threadIdx.x;
+        const int i = e >> lp, sub = e & (P - 1);
+        const uint64_t c = i < m ? cand[i] : 0ull;
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int j = sub;
+        for (; j + 3 * P < m; j += 4 * P) {
+            r0 += cand[j] > c;
+            r1 += cand[j + P] > c;
+            r2 += cand[j + 2 * P] > c;
+            r3 += cand[j + 3 * P] > c;
+        }
+        for (; j < m; j += P) r0 += cand[j] > c;
+        int rk = (r0 + r1) + (r2 + r3);
+        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
+        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
+    }
 }
 
 }  // namespace qsa

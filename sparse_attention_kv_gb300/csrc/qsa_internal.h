@@ -48,7 +48,9 @@ struct WsLayout {
     size_t total;
     int maxch;
 };
-WsLayout ws_layout(int nq, int max_blocks, int k);
+// fused: the candidate arrays hold at least kMergeCap entries per query (the fused
+// select's per-CTA candidate lists)
+WsLayout ws_layout(int nq, int max_blocks, int k, bool fused = false);
 
 struct TopkArgs {
     const float *scores;
@@ -86,8 +88,11 @@ qsa_status launch_topk_split(const TopkArgs &a, const SplitGeom &g, cudaStream_t
 // (ids [nq][k] in place), and the merge of [n_shards][nq][k] candidates into ids.
 qsa_status launch_candidates(const float *scores, int64_t stride, int32_t *ids, float *cand_scores, int nq, int k,
                              int32_t offset, cudaStream_t s);
-qsa_status launch_merge(const float *cand_scores, const int32_t *cand_ids, int n_shards, int nq, int k, int32_t *ids,
-                        cudaStream_t s);
+// counts == nullptr: every slot with id >= 0; else the first counts[q * counts_stride + g]
+// slots of shard g.  Shard g's candidates of query q start at
+// ((g nq) + q) kslot; n_shards * kslot <= kMergeCap.
+qsa_status launch_merge(const float *cand_scores, const int32_t *cand_ids, const int32_t *counts, int counts_stride,
+                        int n_shards, int nq, int kslot, int k, int32_t *ids, cudaStream_t s);
 
 struct ScorerArgs {
     const void *q;
@@ -102,12 +107,15 @@ struct ScorerArgs {
     float *scores;
     int64_t stride;
     uint32_t *flags;
-    // fused score-then-select (fused != 0): scores may be null
+    // fused score-then-select (fused != 0): scores may be null; the CTAs' candidate
+    // lists go to cand_scores / cand_ids (the workspace's ckeys / cids regions) with
+    // their lengths in counts, and a merge kernel writes ids
     bool fused;
     int32_t *ids;
     int k;
-    uint32_t *tickets;
-    uint64_t *cand;   // nq * maxch * k packed candidates; spans the ckeys and cids regions
+    float *cand_scores;
+    int32_t *cand_ids;
+    int32_t *counts;
     int maxch;
 };
 qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s);

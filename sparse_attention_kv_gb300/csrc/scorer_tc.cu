@@ -44,6 +44,7 @@ constexpr int kEpiParts = 4;                  // epilogue warps per TMEM lane qu
 constexpr int kEpi = 128 * kEpiParts;         // epilogue threads
 constexpr int kThreads = 64 + kEpi;           // + one TMA warp and one MMA warp
 constexpr int kMaxChunks = (16 + kEpiParts - 1) / kEpiParts;  // 16-column chunks per thread
+constexpr int kFusedMaxQ = 16;                // queries per group of the fused kernel (scores kept on chip)
 
 template <int DT>
 struct Cfg;
@@ -95,6 +96,7 @@ struct Ctrl {
     int last;
     __align__(16) float w[256];
     int nb[256];
+    uint64_t top[kEpi / 32][32];   // fused form: an epilogue warp's exact top k (k <= 32)
 };
 
 template <int DT, bool FUSED>
@@ -113,11 +115,13 @@ struct KParams {
     int64_t stride;
     uint32_t *flags;
     int nq, bound, qg, bn, tiles_per_cta, tiles_total, tmem_cols;
-    // fused score-then-select only
-    int32_t *ids;
+    // fused score-then-select only: each CTA's candidate lists, [cpg][nq][kslot] scores and
+    // global ids, and their lengths counts[q * maxch + CTA]
     int k;
-    uint32_t *tickets;
-    uint64_t *cand;    // packed candidates; a query group uses nq_group * maxch * k entries from q0 * maxch * k
+    float *cand_scores;
+    int32_t *cand_ids;
+    int32_t *counts;
+    int kslot;
     int maxch;
     int sb_stride;     // scores per query in the on-chip buffer (tiles_per_cta * 128)
 };
@@ -182,143 +186,150 @@ __device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes,
 
 // ---------------------------------------------------------------- fused select
 
-// The selection tail of the fused kernel.  Stage A: each epilogue warp takes the
-// queries j = warp, warp + 16, ... of the group and writes the top min(n_loc, k)
-// of this CTA's blocks of the query to the workspace (descending for k <= 32,
-// else in block order).  The CTA then takes a ticket; the last CTA of the group
-// runs stage B: it loads every chunk's candidates of every query into shared
-// memory (a chunk c holds min(k, max(0, n - c * S)) of them, S = blocks per CTA,
-// so the lists need no counts and concatenate without gaps) and each warp
-// selects its queries' k blocks from them.  A query's selection restricted to one
-// CTA's range of blocks is a prefix of that range's selection order, so every
-// selected block is among its CTA's candidates (the split of Strata PR #3987,
-// section "Approach"), and the result equals selecting from the whole row.
-__device__ __noinline__ void fused_select(const KParams &p, Ctrl &ct, float *sbuf, uint32_t *hist, int q0, int qv,
-                                          int t_begin, int ntiles) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ew = warp - 2;   // epilogue warp index; the TMA and MMA warps only join the barriers
+// The selection step of the fused kernel, stage A.  For each query j of the group
+// (epilogue warp j, j + 16, ...), this CTA's blocks of it are on chip; they are
+// reduced to a list that holds every block of the query's selection among them,
+// written to the workspace as (score, global id) with its length.  The merge kernel
+// launched after this one selects over every CTA's lists.  A query's selection
+// restricted to one CTA's blocks is a prefix of that range's order (the split of
+// Strata PR #3987, section "Approach"), so a list holding the range's k best is
+// enough:
+//  * at most kslot blocks: all of them;
+//  * k <= 32: the scores at or above the k-th largest of the lanes' maxima (k
+//    distinct entries reach it; about 90 of 1,024 on continuous scores), unranked --
+//    the one-read filter of "#2093 sm_75: the prompt path's top-k with one full
+//    read of the scores" (steps 2-3) with the bound taken from the chunk itself;
+//  * more survivors than kslot (heavy ties), or k > 32: the range's exact top k.
+__device__ __noinline__ void fused_stage_a(const KParams &p, Ctrl &ct, float *sbuf, uint32_t *hist, int q0, int qv,
+                                           int t_begin, int ntiles) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ew = warp - 2;   // epilogue warp index
+    if (ew < 0) return;        // the TMA and MMA warps have no part here
     constexpr int nw = kEpi / 32;
-    const int c = blockIdx.x, nch = gridDim.x, g = blockIdx.y;
-    // the parameters live in memory that any store here could alias: read them once
-    const int k = p.k, maxch = p.maxch, sb_stride = p.sb_stride;
-    uint64_t *const __restrict__ cand = p.cand;
-    int32_t *const __restrict__ ids = p.ids;
-    uint32_t *const tickets = p.tickets;
-    // per-warp scratch (1 KB): the fast forms' 64-entry buffer and id slots, or the fallbacks' 256-bin histogram (zero on entry to warp_select)
-    uint32_t *h = hist + (ew > 0 ? ew : 0) * 256;
+    const int c = blockIdx.x;
+    // the parameters live in memory that the stores below could alias: read them once
+    const int k = p.k, kslot = p.kslot, nq = p.nq, sb_stride = p.sb_stride, maxch = p.maxch;
+    float *const __restrict__ cs = p.cand_scores;
+    int32_t *const __restrict__ ci = p.cand_ids;
+    int32_t *const __restrict__ counts = p.counts;
+    uint32_t *h = hist + ew * 256;                        // 1 KB: 64-entry rank buffer or a histogram
     uint64_t *buf = reinterpret_cast<uint64_t *>(h);
-    int32_t *sid = reinterpret_cast<int32_t *>(h + 160);
-    const bool fast = k <= 32;
-    const int S = sb_stride;             // blocks per CTA
-    const int kc = min(k, S);            // candidates of a full chunk
-    const int per = nch * kc;            // candidates of a query
-    // the group's candidates are one contiguous run, query j's list at j * per and
-    // its chunk c at j * per + c * kc: the layout stage B keeps in shared memory
-    uint64_t *const __restrict__ gcand = cand + (size_t)q0 * maxch * k;
-    if (ew >= 0) {
-        for (int i = lane; i < 256; i += 32) h[i] = 0u;
-        __syncwarp();
-        const int lo = t_begin * kBM;
-        for (int j = ew; j < qv; j += nw) {
-            const int q = q0 + j;
-            const int n = ct.nb[j];
-            if (n <= k) continue;   // stage B emits 0..n-1
-            const int nloc = max(0, min(ntiles * kBM, n - lo));
-            uint64_t *dst = gcand + (size_t)j * per + (size_t)c * kc;
-            const float *row = sbuf + (size_t)j * sb_stride;   // this CTA's blocks of query j
-            if (nloc <= k) {
-                for (int i = lane; i < nloc; i += 32) dst[i] = pack_cand(score_key(row[i]), lo + i);
-                if (fast) {   // descending, like the other chunks
-                    __syncwarp();
-                    uint64_t v = lane < nloc ? ~dst[lane] : ~0ull;
-                    __syncwarp();
-                    warp_sort32_asc(v);
-                    if (lane < nloc) dst[lane] = ~v;
+    uint64_t *top = ct.top[ew];
+    const float ninf = __int_as_float(0xff800000);
+    const int lo = t_begin * kBM;
+    for (int j = ew; j < qv; j += nw) {
+        const int q = q0 + j;
+        const int nloc = max(0, min(ntiles * kBM, ct.nb[j] - lo));
+        const size_t base = ((size_t)c * nq + q) * kslot;
+        float *row = sbuf + (size_t)j * sb_stride;   // this CTA's blocks of query j
+        int count = -1;
+        if (nloc <= kslot) {
+            for (int i = lane; i < nloc; i += 32) {
+                cs[base + i] = row[i];
+                ci[base + i] = lo + i;
+            }
+            count = nloc;
+        } else if (k <= 32 && nloc <= 1024) {
+            // lane l holds entries l + 32 t; at least k lanes hold one (nloc > kslot >= k),
+            // the others read -inf
+            float x[32];
+            float mx = ninf;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = row[min(lane + 32 * t, nloc - 1)];   // nloc > kslot >= 1
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                if (lane + 32 * t >= nloc) x[t] = ninf;
+                mx = fmaxf(mx, x[t]);
+            }
+            uint32_t kk = score_key(mx), bk;
+            if (k == 32) {
+                bk = __reduce_min_sync(kFull, kk);
+            } else {
+                bk = 0u;
+                for (int it = 0; it < k; ++it) {
+                    bk = __reduce_max_sync(kFull, kk);
+                    const unsigned win = __ballot_sync(kFull, kk == bk);
+                    if (lane == __ffs(win) - 1) kk = 0u;   // 0 is below every score's key
                 }
-                continue;
             }
-            if (fast) {
-                bool ok;
-                if (nloc <= 128) ok = stage_a_regs<1>(row, nloc, k, lo, buf, dst);
-                else if (nloc <= 256) ok = stage_a_regs<2>(row, nloc, k, lo, buf, dst);
-                else if (nloc <= 512) ok = stage_a_regs<4>(row, nloc, k, lo, buf, dst);
-                else if (nloc <= 1024) ok = stage_a_regs<8>(row, nloc, k, lo, buf, dst);
-                else ok = stage_a_smem(row, nloc, k, lo, buf, dst);
-                if (ok) continue;
+            // each lane counts its survivors, a scan over the lanes places them, and
+            // each lane writes its own run (no vote inside the loop)
+            const float bf = key_float(bk);
+            int cnt = 0;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) cnt += (lane + 32 * t < nloc && x[t] >= bf) ? 1 : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += v;
             }
-            for (int i = lane; i < 256; i += 32) h[i] = 0u;
-            __syncwarp();
-            warp_select([&](int i) { return score_key(row[i]); }, nloc, k, h,
-                        [&](int pos, int i) { dst[pos] = pack_cand(score_key(row[i]), lo + i); });
-            __syncwarp();
-            if (fast) {   // re-sort descending
-                uint64_t v = lane < k ? ~dst[lane] : ~0ull;
-                __syncwarp();
-                warp_sort32_asc(v);
-                if (lane < k) dst[lane] = ~v;
+            const int total = __shfl_sync(kFull, incl, 31);
+            if (total <= kslot) {
+                int at = incl - cnt;
+                if (2 * total <= sb_stride) {
+                    // the row is in registers: its shared copy holds the list (scores,
+                    // then ids), written to the workspace in whole lines
+                    float *st = row;
+                    int32_t *sti = reinterpret_cast<int32_t *>(row + total);
+                    __syncwarp();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int i = lane + 32 * t;
+                        if (i < nloc && x[t] >= bf) {
+                            st[at] = x[t];
+                            sti[at] = lo + i;
+                            ++at;
+                        }
+                    }
+                    __syncwarp();
+                    for (int e = lane; e < total; e += 32) {
+                        cs[base + e] = st[e];
+                        ci[base + e] = sti[e];
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int i = lane + 32 * t;
+                        if (i < nloc && x[t] >= bf) {
+                            cs[base + at] = x[t];
+                            ci[base + at] = lo + i;
+                            ++at;
+                        }
+                    }
+                }
+                count = total;
             }
         }
-    }
-    __syncthreads();
-    if (tid == 0) {   // the barrier orders the CTA's candidate writes before this fence
-        __threadfence();
-        ct.last = atomicAdd(&tickets[g], 1u) == (unsigned)nch - 1u;
-    }
-    __syncthreads();
-    if (!ct.last) return;
-    if (tid == 0) __threadfence();
-    __syncthreads();
-    // every candidate of the group into shared memory, one flat copy (entries a
-    // chunk did not fill are copied too and never read)
-    uint64_t *lists = reinterpret_cast<uint64_t *>(sbuf);
-    {
-        constexpr int kU = 8;   // loads in flight per thread
-        const int total = qv * per;
-        for (int e0 = tid; e0 < total; e0 += kThreads * kU) {
-            uint64_t v[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) v[u] = __ldcg(gcand + min(e0 + u * kThreads, total - 1));
-#pragma unroll
-            for (int u = 0; u < kU; ++u)
-                if (e0 + u * kThreads < total) lists[e0 + u * kThreads] = v[u];
-        }
-    }
-    __syncthreads();
-    if (ew >= 0) {
-        for (int j = ew; j < qv; j += nw) {
-            const int q = q0 + j;
-            const int n = ct.nb[j];
-            int32_t *out = ids + (size_t)q * k;
-            if (n <= k) {
-                for (int i = lane; i < k; i += 32) out[i] = i < n ? i : -1;
-                continue;
+        if (count < 0) {   // the range's exact top k
+            bool ok = false;
+            if (k <= 32) {
+                if (nloc <= 128) ok = stage_a_regs<1>(row, nloc, k, lo, buf, top);
+                else if (nloc <= 256) ok = stage_a_regs<2>(row, nloc, k, lo, buf, top);
+                else if (nloc <= 512) ok = stage_a_regs<4>(row, nloc, k, lo, buf, top);
+                else if (nloc <= 1024) ok = stage_a_regs<8>(row, nloc, k, lo, buf, top);
+                else ok = stage_a_smem(row, nloc, k, lo, buf, top);
+                if (ok) {
+                    __syncwarp();
+                    if (lane < k) {
+                        cs[base + lane] = key_float(cand_key(top[lane]));
+                        ci[base + lane] = cand_id(top[lane]);
+                    }
+                }
             }
-            const int full = n / S;
-            const int L = full * kc + min(kc, n - full * S);   // n <= nch * S
-            const uint64_t *list = lists + (size_t)j * per;
-            if (fast) {
-                if (L > k && stage_b_fast(list, nch, kc, S, n, k, buf, sid, out)) continue;
-                // exact 64-bit selection (no ties: packed values are distinct), then ids ascending
+            if (!ok) {   // heavy ties, or k > 32: the radix warp select over the range
                 for (int i = lane; i < 256; i += 32) h[i] = 0u;
                 __syncwarp();
-                warp_select([&](int i) { return list[i]; }, L, k, h, [&](int pos, int i) { out[pos] = cand_id(list[i]); });
-                __syncwarp();
-                int32_t id = lane < min(L, k) ? out[lane] : 0x7fffffff;
-                __syncwarp();
-                warp_sort32_asc(id);
-                if (lane < k) out[lane] = lane < L ? id : -1;
-                __syncwarp();
-                continue;
+                warp_select([&](int i) { return score_key(row[i]); }, nloc, k, h, [&](int at, int i) {
+                    cs[base + at] = row[i];
+                    ci[base + at] = lo + i;
+                });
             }
-            for (int i = lane; i < 256; i += 32) h[i] = 0u;
-            __syncwarp();
-            warp_select([&](int i) { return cand_key(list[i]); }, L, k, h,
-                        [&](int pos, int i) { out[pos] = cand_id(list[i]); });
-            __syncwarp();
+            count = k;
         }
+        __syncwarp();
+        if (lane == 0) counts[(size_t)q * maxch + c] = count;
     }
-    __syncthreads();
-    if (tid == 0) tickets[g] = 0u;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -576,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     }  // ntiles > 0
     if (tid == 0 && ct.abort && p.flags) atomicOr(p.flags, QSA_FLAG_WAIT_TIMEOUT);
-    if constexpr (FUSED) fused_select(p, ct, sbuf, hist, q0, qv, t_begin, max(ntiles, 0));
+    if constexpr (FUSED) fused_stage_a(p, ct, sbuf, hist, q0, qv, t_begin, max(ntiles, 0));
 }
 
 // ---------------------------------------------------------------- host side
@@ -632,10 +643,11 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     const int sms = num_sms();
     const int t1 = std::max(tiles, 1);
     // queries per group: as many as fill the MMA's N side; the fused kernel keeps at
-    // most 16 on chip (one epilogue warp each) and fewer when their scores or the
-    // merge candidates would not fit
-    int qg = std::min(a.nq, std::max(1, a.fused ? std::min(max_bn / H, kEpi / 32) : max_bn / H));
-    int groups = 0, cpg = 0, tpc = 0;
+    // most 16 on chip and fewer when their scores would not fit.  Its CTAs' candidate
+    // lists (kslot slots each) share the workspace's candidate arrays, and the merge
+    // holds the cpg lists of a query on chip.
+    int qg = std::min(a.nq, std::max(1, a.fused ? std::min(max_bn / H, kFusedMaxQ) : max_bn / H));
+    int groups = 0, cpg = 0, tpc = 0, kslot = 0;
     for (;; qg = (qg + 1) / 2) {
         groups = (a.nq + qg - 1) / qg;
         cpg = std::max(1, std::min(t1, sms / groups));
@@ -649,14 +661,19 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
         if (fits) {
             tpc = std::min(tpc, tpc_max);
             cpg = (t1 + tpc - 1) / tpc;
-            const long kc = std::min(a.k, tpc * kBM);   // candidates of a full chunk
-            fits = (long)qg * cpg * kc * 8 <= sbuf && cpg <= a.maxch;
+            if ((long)cpg * a.k > kMergeCap) {   // fewer CTAs per group, more tiles each
+                tpc = (t1 + std::max(1, kMergeCap / a.k) - 1) / std::max(1, kMergeCap / a.k);
+                cpg = (t1 + tpc - 1) / tpc;
+                fits = tpc <= tpc_max;
+            }
+            kslot = kMergeCap / cpg;   // the fused workspace holds kMergeCap candidates per query
+            fits = fits && kslot >= a.k;
         }
         if (fits) break;
         if (qg == 1)
             return fail(QSA_ERR_UNSUPPORTED,
-                        "fused select: the per-CTA scores or the %d x k = %d merge candidates do not fit on chip; "
-                        "use the chained form", cpg, a.k);
+                        "fused select: the per-CTA scores do not fit on chip, or %d CTAs x k = %d candidates exceed "
+                        "the merge's %d; use the chained form", cpg, a.k, kMergeCap);
     }
     cpg = (t1 + tpc - 1) / tpc;
     const int bn = (qg * H + 15) / 16 * 16;
@@ -683,24 +700,32 @@ qsa_status launch_scorer(const ScorerArgs &a, cudaStream_t s) {
     kp.tiles_per_cta = tpc;
     kp.tiles_total = tiles;
     kp.tmem_cols = tmem_cols;
-    kp.ids = a.ids;
     kp.k = a.k;
-    kp.tickets = a.tickets;
-    kp.cand = a.cand;
     kp.maxch = a.maxch;
     kp.sb_stride = tpc * kBM;
+    kp.cand_scores = a.cand_scores;
+    kp.cand_ids = a.cand_ids;
+    kp.counts = a.counts;
+    kp.kslot = kslot;
     const dim3 grid(cpg, groups);
     switch (dt) {
     case QSA_F32:
-        return a.fused ? launch_heads<QSA_F32, true>(H, mk, mq, kp, grid, s)
-                       : launch_heads<QSA_F32, false>(H, mk, mq, kp, grid, s);
+        st = a.fused ? launch_heads<QSA_F32, true>(H, mk, mq, kp, grid, s)
+                     : launch_heads<QSA_F32, false>(H, mk, mq, kp, grid, s);
+        break;
     case QSA_E4M3:
-        return a.fused ? launch_heads<QSA_E4M3, true>(H, mk, mq, kp, grid, s)
-                       : launch_heads<QSA_E4M3, false>(H, mk, mq, kp, grid, s);
+        st = a.fused ? launch_heads<QSA_E4M3, true>(H, mk, mq, kp, grid, s)
+                     : launch_heads<QSA_E4M3, false>(H, mk, mq, kp, grid, s);
+        break;
     default:
-        return a.fused ? launch_heads<QSA_BF16, true>(H, mk, mq, kp, grid, s)
-                       : launch_heads<QSA_BF16, false>(H, mk, mq, kp, grid, s);
+        st = a.fused ? launch_heads<QSA_BF16, true>(H, mk, mq, kp, grid, s)
+                     : launch_heads<QSA_BF16, false>(H, mk, mq, kp, grid, s);
+        break;
     }
+    if (st != QSA_OK || !a.fused) return st;
+    // the fused form's last step: one CTA per query selects over its CTAs' lists,
+    // launched as a programmatic dependent (its launch overlaps the scorer's work)
+    return launch_merge(a.cand_scores, a.cand_ids, a.counts, a.maxch, cpg, a.nq, kslot, a.k, a.ids, s);
 }
 
 }  // namespace qsa

@@ -44,39 +44,78 @@ struct __align__(16) MergeSmem {
     uint32_t key[kMergeCap];
     int32_t id[kMergeCap];
     int32_t sel[1024];
+    uint64_t cand[kMergeNT];   // k <= 32: the candidates at or above the bound, packed
+    uint32_t wb[kMergeNT / 32];
+    int nsurv;
 };
 
-// Stage B: one CTA per query.  The query's candidates of every shard (id >= 0) go
-// to shared memory as (key, id); the threshold T (the k-th largest key), the keys
-// above it and, of the keys equal to it, the lowest ids give the k selected
-// blocks (the rule of "#2093 sm_75: the prompt path's top-k with one full read of
-// the scores", step 3), emitted in ascending id order and -1 padded.
+// Stage B: one CTA per query.  The query's candidates of every shard (id >= 0; with
+// counts, the first counts[q * counts_stride + g] of shard g) go to shared memory as
+// (key, id); the threshold T (the k-th largest key), the keys above it and, of the
+// keys equal to it, the lowest ids give the k selected blocks (the rule of "#2093
+// sm_75: the prompt path's top-k with one full read of the scores", step 3),
+// emitted in ascending id order and -1 padded.  Shard g's candidates of query q
+// start at ((g nq) + q) kslot.
 __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict__ cand_scores,
-                                                         const int32_t *__restrict__ cand_ids, int n_shards, int nq,
-                                                         int k, int32_t *__restrict__ out_ids) {
+                                                         const int32_t *__restrict__ cand_ids,
+                                                         const int32_t *__restrict__ counts, int counts_stride,
+                                                         int n_shards, int nq, int kslot, int k,
+                                                         int32_t *__restrict__ out_ids) {
     wait_prior_grid();   // the candidates may come from the kernel launched just before
     allow_dependent_launch();
     __shared__ MergeSmem sm;
-    const int q = blockIdx.x;
+    const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     cand_smem_init(sm.cs);
-    __syncthreads();
-    const int total = n_shards * k;
+    if (threadIdx.x == 0) sm.nsurv = 0;
+    // every slot of this thread (slots t, t + 256, ... of the shard-major list) and its
+    // list's length loaded at once (a slot outside the lists reads slot 0 and is
+    // dropped), so that all of the loads are in flight together
+    constexpr int PER = kMergeCap / kMergeNT;
+    const int total = n_shards * kslot;   // <= kMergeCap
+    float sc[PER];
+    int32_t cid[PER], len[PER], slot[PER];
+    size_t off[PER];
+    // slot e = r * 256 + t is slot i of list g; one division, then steps of 256 slots
+    const int step_g = kMergeNT / kslot, step_i = kMergeNT - step_g * kslot;
+    int g = (int)threadIdx.x / kslot, i = (int)threadIdx.x - g * kslot;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const bool in = r * kMergeNT + (int)threadIdx.x < total;
+        off[r] = in ? ((size_t)g * nq + q) * kslot + i : 0;
+        slot[r] = in ? i : kslot;   // kslot: never below a list's length
+        len[r] = (int)min(g, n_shards - 1);
+        g += step_g;
+        i += step_i;
+        if (i >= kslot) {
+            i -= kslot;
+            ++g;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        cid[r] = cand_ids[off[r]];
+        sc[r] = cand_scores[off[r]];
+        len[r] = counts ? counts[(size_t)q * counts_stride + len[r]] : kslot;
+    }
+    __syncthreads();   // the counters above are set (the loads stay in flight)
+#pragma unroll
+    for (int r = 0; r < PER; ++r)
+        if (slot[r] >= len[r]) cid[r] = -1;
+    int nv = 0;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) nv += cid[r] >= 0;
+    int pos = warp_append(nv, &sm.cs.cnt[2]);
     uint32_t mn = 0xffffffffu, mx = 0u;
-    for (int base = 0; base < total; base += kMergeNT) {
-        const int e = base + (int)threadIdx.x;
-        const int g = e / k, i = e - (e / k) * k;
-        const size_t off = ((size_t)g * nq + q) * k + i;
-        const int32_t id = e < total ? cand_ids[off] : -1;
-        const bool v = id >= 0;
-        const int pos = warp_append(v ? 1 : 0, &sm.cs.cnt[2]);
-        if (v) {
-            const uint32_t key = score_key(cand_scores[off]);
+#pragma unroll
+    for (int r = 0; r < PER; ++r)
+        if (cid[r] >= 0) {
+            const uint32_t key = score_key(sc[r]);
             sm.key[pos] = key;
-            sm.id[pos] = id;
+            sm.id[pos] = cid[r];
+            ++pos;
             mn = min(mn, key);
             mx = max(mx, key);
         }
-    }
     block_minmax<kMergeNT>(mn, mx, sm.cs);
     const int m = sm.cs.cnt[2];
     int32_t *out = out_ids + (size_t)q * k;
@@ -85,6 +124,50 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict
         __syncthreads();
         sort_emit<kMergeNT>(sm.sel, m, k, out);
         return;
+    }
+    if (k <= 32) {
+        // A bound first, as in the warp top-k: thread t's candidates are t, t + 256, ...;
+        // each warp takes the r-th largest of its threads' maxima (r = ceil(k / 8)) and
+        // the bound is the smallest of those, so at least k candidates reach it.  The few
+        // that do are ranked exactly on (key, ~id), the selection order.  Fewer than 256
+        // candidates: all of them are ranked.
+        if (m <= kMergeNT) {
+            for (int i = threadIdx.x; i < m; i += kMergeNT) sm.cand[i] = pack_cand(sm.key[i], sm.id[i]);
+            if (threadIdx.x == 0) sm.nsurv = m;
+        } else {
+            uint32_t tm = 0u;   // every thread holds a candidate (m > 256)
+            for (int i = threadIdx.x; i < m; i += kMergeNT) tm = max(tm, sm.key[i]);
+            const int r = (k + kMergeNT / 32 - 1) / (kMergeNT / 32);
+            uint32_t res = 0u;
+            for (int it = 0; it < r; ++it) {
+                res = __reduce_max_sync(kFull, tm);
+                const unsigned win = __ballot_sync(kFull, tm == res);
+                if (lane == __ffs(win) - 1) tm = 0u;   // 0 is below every score's key
+            }
+            if (lane == 0) sm.wb[warp] = res;
+            __syncthreads();
+            uint32_t B = 0xffffffffu;
+#pragma unroll
+            for (int w = 0; w < kMergeNT / 32; ++w) B = min(B, sm.wb[w]);
+            for (int i = threadIdx.x; i < m; i += kMergeNT)
+                if (sm.key[i] >= B) {
+                    const int p = atomicAdd(&sm.nsurv, 1);
+                    if (p < kMergeNT) sm.cand[p] = pack_cand(sm.key[i], sm.id[i]);
+                }
+        }
+        __syncthreads();
+        const int m2 = sm.nsurv;
+        if (m2 <= kMergeNT) {
+            rank_survivors<kMergeNT>(sm.cand, m2, k, sm.sel);
+            __syncthreads();
+            if (warp == 0) {
+                int v = lane < k ? sm.sel[lane] : 0x7fffffff;
+                warp_sort32_asc(v);
+                if (lane < k) out[lane] = v;
+            }
+            return;
+        }
+        // heavy ties at the bound: the exact select below
     }
     const Threshold th = smem_threshold<kMergeNT>(
         [&](int i, uint32_t &key) {
@@ -122,10 +205,10 @@ qsa_status launch_candidates(const float *scores, int64_t stride, int32_t *ids, 
                       cand_scores, nq, k, offset);
 }
 
-qsa_status launch_merge(const float *cand_scores, const int32_t *cand_ids, int n_shards, int nq, int k, int32_t *ids,
-                        cudaStream_t s) {
+qsa_status launch_merge(const float *cand_scores, const int32_t *cand_ids, const int32_t *counts, int counts_stride,
+                        int n_shards, int nq, int kslot, int k, int32_t *ids, cudaStream_t s) {
     return launch_pdl("merge_kernel launch", merge_kernel, dim3(nq), dim3(kMergeNT), s, cand_scores, cand_ids,
-                      n_shards, nq, k, ids);
+                      counts, counts_stride, n_shards, nq, kslot, k, ids);
 }
 
 }  // namespace qsa

@@ -98,11 +98,6 @@ constexpr int kNT = 256;   // threads of the register, sample and split kernels
 
 __device__ __forceinline__ float nan_pad() { return __int_as_float(0x7fffffff); }
 
-// Inverse of score_key (for keys of non-NaN scores).
-__device__ __forceinline__ float key_float(uint32_t key) {
-    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
-}
-
 // Row values striped over the block: round r, thread t, component e holds
 // position r*kNT*4 + t*4 + e.  Positions at or past n read as NaN, which no
 // comparison selects.  float4 streaming loads when the row is 16-byte aligned.
@@ -571,50 +566,6 @@ __device__ __noinline__ void warp_chunk_select(const float *row, int n, int k, i
         int below = 0;
         for (int t = 0; t < k; ++t) below += sm.sel[t] < id;
         out[below] = id;
-    }
-}
-
-// Exact ranks of m distinct packed candidates cand[0..m) (rank 0 = the largest):
-// sel[r] = the id of the candidate of rank r, for r < k (exactly k rank below k when
-// m >= k).  A rank is the number of candidates above; P threads per candidate (a
-// power of two dividing the warp) share the count.  Every thread of the NT-thread
-// block calls it.
-template <int NT>
-__device__ __forceinline__ void rank_survivors(const uint64_t *cand, int m, int k, int32_t *sel) {
-    if (m <= 64) {   // the common case: every compare unrolled, P fixed
-        constexpr int P = NT / 64;
-        const int i = (int)threadIdx.x / P, sub = (int)threadIdx.x % P;
-        const uint64_t c = i < m ? cand[i] : 0ull;
-        int rk = 0;
-#pragma unroll
-        for (int t = 0; t < 64 / P; ++t) {
-            const int j = sub + P * t;
-            rk += j < m && cand[j] > c;
-        }
-#pragma unroll
-        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
-        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
-        return;
-    }
-    int lp = 0;   // P = 1 << lp <= 8, as many as the block holds
-    while (lp < 3 && (2 * m << lp) <= NT) ++lp;
-    const int P = 1 << lp;
-    for (int b0 = 0; b0 < m * P; b0 += NT) {
-        const int e = b0 + (int)threadIdx.x;
-        const int i = e >> lp, sub = e & (P - 1);
-        const uint64_t c = i < m ? cand[i] : 0ull;
-        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        int j = sub;
-        for (; j + 3 * P < m; j += 4 * P) {
-            r0 += cand[j] > c;
-            r1 += cand[j + P] > c;
-            r2 += cand[j + 2 * P] > c;
-            r3 += cand[j + 3 * P] > c;
-        }
-        for (; j < m; j += P) r0 += cand[j] > c;
-        int rk = (r0 + r1) + (r2 + r3);
-        for (int o = 1; o < P; o <<= 1) rk += __shfl_xor_sync(kFull, rk, o);
-        if (sub == 0 && i < m && rk < k) sel[rk] = cand_id(c);
     }
 }
 

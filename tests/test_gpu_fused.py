@@ -107,20 +107,36 @@ def test_fused_without_scores_and_workspace_reuse():
     ids1, none, ws = run(case, fused=True, with_scores=False)
     assert none is None
     np.testing.assert_array_equal(ids1, ids_c)
-    for _ in range(3):   # tickets are left at zero: the same workspace works again
+    for _ in range(3):   # the same workspace serves the next calls (no state carries over)
         ids2, _, _ = run(case, fused=True, with_scores=False, ws=ws)
         np.testing.assert_array_equal(ids2, ids_c)
 
 
-def test_fused_rejects_shapes_that_do_not_fit_and_forced_paths():
+def test_fused_large_k_long_rows_takes_more_tiles_per_cta():
+    """k = 1,024 over 60,000 blocks: the merge holds at most 4,096 candidates per query,
+    so the fused form gives each CTA more tiles (and fewer CTAs per query)."""
     case = inputs.make_case(8300, 4, 16, 60000, inputs.BF16, 64 * 60000, 1024, active_blocks=60000)
+    ids_c, _, _ = run(case, fused=False)
+    ids_f, _, _ = run(case, fused=True, with_scores=False)
+    np.testing.assert_array_equal(ids_f, ids_c)
+
+
+def test_fused_rejects_shapes_that_do_not_fit_and_forced_paths():
+    # 100,000 blocks at k = 1,024: four CTAs per query at most, each would hold more
+    # scores than its shared memory
+    case = inputs.make_case(8301, 4, 16, 100000, inputs.BF16, 64 * 100000, 1024, active_blocks=100000)
     with pytest.raises(qsa.QSAError) as e:
         run(case, fused=True, with_scores=False)
     assert e.value.status == qsa.ERR_UNSUPPORTED
     small = inputs.decode_case(0)
     q, w, kb, nb = parity.to_device(small)
     ids = torch.empty((small.nq, small.k), dtype=torch.int32, device="cuda")
-    ws = qsa.alloc_workspace(small.nq, small.max_blocks, small.k)
+    ws = qsa.alloc_workspace(small.nq, small.max_blocks, small.k, fused=True)
     with pytest.raises(qsa.QSAError) as e:
         qsa.select(q, w, kb, nb, small.k, ids, ws, fused=True, path=qsa.PATH_SAMPLE)
     assert e.value.status == qsa.ERR_UNSUPPORTED
+    # the fused form's candidate lists need the fused workspace size
+    small_ws = qsa.alloc_workspace(small.nq, small.max_blocks, small.k)
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.select(q, w, kb, nb, small.k, ids, small_ws, fused=True)
+    assert e.value.status == qsa.ERR_WORKSPACE
