@@ -67,9 +67,9 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict
     const int q = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     cand_smem_init(sm.cs);
     if (threadIdx.x == 0) sm.nsurv = 0;
-    // every slot of this thread (slots t, t + 256, ... of the shard-major list) and its
-    // list's length loaded at once (a slot outside the lists reads slot 0 and is
-    // dropped), so that all of the loads are in flight together
+    // the lengths of this thread's lists first, then the loads of every slot of this
+    // thread that holds a candidate (slots t, t + 256, ... of the shard-major list) at
+    // once, so that they are all in flight together
     constexpr int PER = kMergeCap / kMergeNT;
     const int total = n_shards * kslot;   // <= kMergeCap
     float sc[PER];
@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
         const bool in = r * kMergeNT + (int)threadIdx.x < total;
-        off[r] = in ? ((size_t)g * nq + q) * kslot + i : 0;
-        slot[r] = in ? i : kslot;   // kslot: never below a list's length
+        off[r] = ((size_t)g * nq + q) * kslot + i;
+        slot[r] = in ? i : kslot;   // kslot: at or past every list's length
         len[r] = (int)min(g, n_shards - 1);
         g += step_g;
         i += step_i;
@@ -92,15 +92,14 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict
         }
     }
 #pragma unroll
-    for (int r = 0; r < PER; ++r) {
-        cid[r] = cand_ids[off[r]];
-        sc[r] = cand_scores[off[r]];
-        len[r] = counts ? counts[(size_t)q * counts_stride + len[r]] : kslot;
-    }
-    __syncthreads();   // the counters above are set (the loads stay in flight)
+    for (int r = 0; r < PER; ++r) len[r] = counts ? counts[(size_t)q * counts_stride + len[r]] : kslot;
 #pragma unroll
-    for (int r = 0; r < PER; ++r)
-        if (slot[r] >= len[r]) cid[r] = -1;
+    for (int r = 0; r < PER; ++r) {
+        const bool v = slot[r] < len[r];
+        cid[r] = v ? cand_ids[off[r]] : -1;
+        sc[r] = v ? cand_scores[off[r]] : 0.0f;
+    }
+    __syncthreads();   // the counters above are set
     int nv = 0;
 #pragma unroll
     for (int r = 0; r < PER; ++r) nv += cid[r] >= 0;
