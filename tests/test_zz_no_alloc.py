@@ -60,6 +60,26 @@ def test_static_entry_matches_workspace_entry_on_two_calls(shape):
         np.testing.assert_array_equal(got.cpu().numpy(), oracle.select_f32(sc, nb, k))
 
 
+def test_static_entry_leaves_device_memory_unchanged():
+    """After one call (which loads the kernels and looks up the scratch's address), more
+    calls take no device memory: the free bytes the driver reports do not move."""
+    lib = qsa.load()
+    nq, C, k = 64, 4096, 32
+    sc = inputs.normal_scores(9300, nq, C)
+    scores = torch.from_numpy(sc).cuda()
+    nb = np.full(nq, C, dtype=np.int32)
+    n_dev = torch.from_numpy(nb).cuda()
+    ids = torch.empty((nq, k), dtype=torch.int32, device="cuda")
+    assert _call_static(lib, scores, n_dev, k, ids, C, -1, qsa.PATH_AUTO) == qsa.OK
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        assert _call_static(lib, scores, n_dev, k, ids, C, -1, qsa.PATH_AUTO) == qsa.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    np.testing.assert_array_equal(ids.cpu().numpy(), oracle.select_f32(sc, nb, k))
+
+
 def test_static_entry_rejects_sizes_beyond_its_scratch():
     lib = qsa.load()
     nq, C, k = 256, 8192, 1024
