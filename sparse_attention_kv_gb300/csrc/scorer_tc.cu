@@ -196,7 +196,7 @@ __device__ __forceinline__ void split_tf32(uint8_t *buf, uint8_t *lo, int bytes,
 // enough:
 //  * at most kslot blocks: all of them;
 //  * k <= 32: the scores at or above the k-th largest of the lanes' maxima (k
-//    distinct entries reach it; about 90 of 1,024 on continuous scores), unranked --
+//    distinct entries reach it; about 120 of 1,024 on continuous scores), unranked --
 //    the one-read filter of "#2093 sm_75: the prompt path's top-k with one full
 //    read of the scores" (steps 2-3) with the bound taken from the chunk itself;
 //  * more survivors than kslot (heavy ties), or k > 32: the range's exact top k.
