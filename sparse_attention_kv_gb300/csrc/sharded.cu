@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const float *__restrict
         const bool in = r * kMergeNT + (int)threadIdx.x < total;
         off[r] = ((size_t)g * nq + q) * kslot + i;
         slot[r] = in ? i : kslot;   // kslot: at or past every list's length
-        len[r] = (int)min(g, n_shards - 1);
+        len[r] = min(g, n_shards - 1);   // the slot's list for now; its length below
         g += step_g;
         i += step_i;
         if (i >= kslot) {
