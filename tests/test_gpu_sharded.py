@@ -146,3 +146,30 @@ def test_merge_of_hand_written_candidates():
     ci2 = torch.tensor([[[7, -1, -1, -1]], [[3, -1, -1, -1]]], dtype=torch.int32, device="cuda")
     qsa.merge_candidates(cs, ci2, ids)
     np.testing.assert_array_equal(ids.cpu().numpy(), [[3, 7, -1, -1]])
+
+
+@pytest.mark.parametrize("G,k", [(128, 32), (4096, 1), (64, 64), (8, 512)])
+def test_merge_at_its_capacity(G, k):
+    """G x k = 4,096 candidates per query (the merge's capacity), on random lists with
+    empty slots: the ids are the oracle's selection over the union of the lists."""
+    nq = 6
+    rng = np.random.default_rng(9700 + G + k)
+    # distinct global ids; scores on a coarse grid so that ties across shards occur
+    ids_all = rng.permutation(G * k * 4)[: G * k].reshape(G, 1, k).repeat(nq, axis=1).astype(np.int32)
+    sc = (rng.integers(0, 50, size=(G, nq, k)) / 8.0).astype(np.float32)
+    empty = rng.random((G, nq, k)) < 0.2
+    ids_all = np.where(empty, -1, ids_all).astype(np.int32)
+    sc = np.where(empty, -np.inf, sc).astype(np.float32)
+    cs = torch.from_numpy(sc).cuda()
+    ci = torch.from_numpy(ids_all).cuda()
+    ids = torch.full((nq, k), -7, dtype=torch.int32, device="cuda")
+    qsa.merge_candidates(cs, ci, ids)
+    # the oracle's selection over dense rows that hold each candidate's score at its id
+    # and -inf elsewhere (every row has far more than k candidates)
+    n = G * k * 4
+    rows = np.full((nq, n), -np.inf, dtype=np.float32)
+    for qi in range(nq):
+        v = ids_all[:, qi, :] >= 0
+        rows[qi, ids_all[:, qi, :][v]] = sc[:, qi, :][v]
+    want = oracle.select_f32(rows, np.full(nq, n, dtype=np.int32), k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), want)
