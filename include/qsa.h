@@ -244,13 +244,18 @@ qsa_status qsa_merge_candidates(const float *cand_scores, const int32_t *cand_id
  *
  * fused == 0 (chained): the scorer writes `scores` (required), then the top-k
  *   reads them; both are the calls above.
- * fused != 0: one kernel.  The scorer's epilogue keeps each CTA's block range of
- *   scores on chip, one warp per query picks that range's k candidates, and the
- *   last CTA of a query group to finish merges them (no CTA waits for another);
- *   the scores never go to HBM.  `scores` may be NULL; when given, it also
- *   receives the scores (the same values the chained scorer writes).  `path`
- *   must be QSA_PATH_AUTO.  Shapes whose per-CTA scores or candidates do not fit
- *   on chip (large k, very long contexts) return QSA_ERR_UNSUPPORTED; use the
+ * fused != 0: the scores never go to HBM.  The scorer keeps each CTA's block
+ *   range of scores on chip and, per query, one warp lists every block of that
+ *   range that can be in the selection (the scores at or above the k-th largest
+ *   lane maximum for k <= 32, else the range's exact top k) in the workspace with
+ *   the list's length; a merge kernel, launched as its programmatic dependent
+ *   with one CTA per query, selects over the lists (a query's selection
+ *   restricted to a range is a prefix of that range's order: Strata PR #3987,
+ *   section "Approach").  No CTA waits for another.  `scores` may be NULL; when
+ *   given, it also receives the scores (the same values the chained scorer
+ *   writes).  `path` must be QSA_PATH_AUTO.  Shapes whose per-CTA scores do not
+ *   fit on chip, or whose lists exceed the merge's 4,096 candidates per query
+ *   (large k with very long contexts), return QSA_ERR_UNSUPPORTED; use the
  *   chained form for those.
  * Arguments as in qsa_block_scores / qsa_block_topk; ws must hold
  * qsa_workspace_bytes(nq, max_blocks, k, fused) bytes.
