@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A dependent grid (the top-k of a chained select) launches once every CTA of this
     // grid has executed this or exited, so no scorer CTA is still waiting for an SM
     // when top-k CTAs take free ones; they wait at entry until this grid completes.
+    // This grid is itself launched as a programmatic dependent of the work before it:
+    // the set-up below (TMEM, barriers, tensor-map prefetch) may overlap that work,
+    // and nothing the caller wrote is read, nor the scores written, before the wait.
     allow_dependent_launch();
     const int g = blockIdx.y;
     const int q0 = g * p.qg;
@@ -394,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    wait_prior_grid();   // inputs and the scores buffer may belong to the work before
     // The query tile and the first stages are requested at once.  The tiles run to the
     // host-visible bound: the TMA and MMA warps never wait for n_blocks, and the
     // epilogue stores only the rows below each query's count.
@@ -615,8 +619,18 @@ qsa_status launch_typed(const CUtensorMap &mk, const CUtensorMap &mq, const KPar
             opted_in[dev] = true;
         }
     }
-    scorer_tc_kernel<DT, H, FUSED><<<grid, kThreads, bytes, s>>>(mk, mq, kp);
-    return check_cuda(cudaGetLastError(), FUSED ? "fused scorer+select launch" : "scorer_tc_kernel launch");
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, scorer_tc_kernel<DT, H, FUSED>, mk, mq, kp),
+                      FUSED ? "fused scorer+select launch" : "scorer_tc_kernel launch");
 }
 
 template <int DT, bool FUSED>
