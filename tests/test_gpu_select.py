@@ -210,3 +210,33 @@ def test_fp32_inputs_at_scale_chained_and_fused():
 def test_every_path_end_to_end_on_the_deep_prompt(path):
     """The 256-query, 520,000-token prompt through each top-k path that holds its rows."""
     full_check(inputs.deep_case(2), path)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_back_to_back_selects_share_the_scores_buffer(fused):
+    """Two chained selects enqueued back to back with no host step between them, on one
+    scores buffer and one workspace: the second call's scorer is a programmatic
+    dependent of the first call's top-k (which lets dependents launch at its entry), so
+    it must not read its inputs or overwrite the scores before that top-k has read them
+    (fused: the next scorer's candidate lists wait for the merge before them).  Each
+    call's ids must be the oracle's selection over its own scores."""
+    a, b = inputs.deep_case(0), inputs.deep_case(2)
+    qa, wa, kba, nba = parity.to_device(a)
+    qb, wb, kbb, nbb = parity.to_device(b)
+    C = a.max_blocks
+    ws = qsa.alloc_workspace(a.nq, C, a.k, fused=fused)
+    ref = []
+    for q, w, kb, nb, case in ((qa, wa, kba, nba, a), (qb, wb, kbb, nbb, b)):
+        sc = torch.empty((case.nq, C), device="cuda")
+        qsa.block_scores(q, w, kb, nb, sc, active_blocks=case.active_blocks, ws=ws)
+        torch.cuda.synchronize()
+        ref.append(oracle.select_f32(sc.cpu().numpy(), nb.cpu().numpy(), case.k))
+    shared = torch.full((a.nq, C), float("nan"), device="cuda")
+    outs = [torch.full((a.nq, a.k), -7, dtype=torch.int32, device="cuda") for _ in range(10)]
+    for i, ids in enumerate(outs):
+        q, w, kb, nb, case = (qa, wa, kba, nba, a) if i % 2 == 0 else (qb, wb, kbb, nbb, b)
+        qsa.select(q, w, kb, nb, case.k, ids, ws, scores=shared, fused=fused, active_blocks=case.active_blocks)
+    torch.cuda.synchronize()
+    assert qsa.read_flags(ws) & qsa.ERROR_FLAGS == 0
+    for i, ids in enumerate(outs):
+        np.testing.assert_array_equal(ids.cpu().numpy(), ref[i % 2], err_msg=f"call {i}")
