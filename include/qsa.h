@@ -136,9 +136,8 @@ qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, qsa_stream stream);
  * indexer keys (and queries) in 8 bits, as the pages' engine stores its KV cache
  * in 8 bits ("--kv int8"); the tensor-core 8-bit format of this GPU is e4m3.
  * Launch: the kernel is launched as a programmatic dependent of the work before it
- * on `stream`: its set-up (barriers, tensor memory) may overlap that work, and it
- * reads nothing the caller wrote, and writes no score, until that work has
- * completed.
+ * on `stream`: its CTAs may be scheduled while that work drains, and wait at entry,
+ * before they take tensor memory or touch any buffer, until it has completed.
  * Errors: QSA_ERR_INVALID_ARG for NULL q/w/kblk/n_blocks/scores, nq < 1,
  * head_dim != 128, unsupported n_heads, max_blocks outside [1, QSA_MAX_BLOCKS],
  * scores_stride < max_blocks, misaligned q/kblk, a dtype other than QSA_F32,

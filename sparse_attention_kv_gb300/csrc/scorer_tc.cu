@@ -357,9 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // grid has executed this or exited, so no scorer CTA is still waiting for an SM
     // when top-k CTAs take free ones; they wait at entry until this grid completes.
     // This grid is itself launched as a programmatic dependent of the work before it:
-    // the set-up below (TMEM, barriers, tensor-map prefetch) may overlap that work,
-    // and nothing the caller wrote is read, nor the scores written, before the wait.
+    // its CTAs may be scheduled while that work drains, and each waits here, before it
+    // takes tensor memory or reads or writes anything, until that work has completed.
     allow_dependent_launch();
+    wait_prior_grid();
     const int g = blockIdx.y;
     const int q0 = g * p.qg;
     const int qv = min(p.qg, p.nq - q0);  // queries of this group
@@ -397,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    wait_prior_grid();   // inputs and the scores buffer may belong to the work before
     // The query tile and the first stages are requested at once.  The tiles run to the
     // host-visible bound: the TMA and MMA warps never wait for n_blocks, and the
     // epilogue stores only the rows below each query's count.
